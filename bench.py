@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Throughput of exact tiled attention on GB300, printed as one JSON line.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+the forward (fa_fwd) and, where the library has it, the backward by
+recomputation (fa_bwd) on the same batch, on the long-sequence,
+large-logit workload (B=2, H=16, N=8192, d=128, bf16, Q and K drawn x8).
+``value`` is TFLOP/s under the attention flop convention: 4*B*H*N^2*d for the
+forward plus 2.5x that for the backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU as an
+independent replica (heads are independent problems: no data-path
+collective); the slowest rank's time sets the step time and rank 0 prints.
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3, help="workload index (configs.WORKLOADS)")
+    ap.add_argument("--no-bwd", action="store_true", help="forward only")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic figure (only while the kernel source is unchanged since capture)
+# ---------------------------------------------------------------------------
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "exact_tiled_attention_02_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "exact_tiled_attention_02_gb300", "csrc", "sm103.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(summary: str, source: str):
+    """Per-launch DRAM bytes recorded in a profiles/ summary, if the summary's
+    source hash matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    want = kernel_source_hash(source)
+    meta = {}
+    for ln in text.splitlines():
+        if ln.startswith("bench-key:"):
+            for kv in ln[len("bench-key:"):].split():
+                k, _, v = kv.partition("=")
+                meta[k] = v
+    if meta.get("source_sha") != want:
+        return None
+    try:
+        return float(meta["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, q, k, v, do, with_bwd, budget_s: float, max_heads=None):
+    """Times the float64 oracle head by head until ``budget_s`` is spent;
+    returns (flops done, seconds, heads)."""
+    import numpy as np
+
+    import oracle
+
+    flops_head_f = w.fwd_flops() / (w.B * w.H)
+    done_f, t_total, heads = 0.0, 0.0, 0
+    order = [(b, h) for b in range(w.B) for h in range(w.H)]
+    for b, h in order:
+        if max_heads is not None and heads >= max_heads:
+            break
+        qh = q[b, h].float().numpy().astype(np.float64)
+        kh = k[b, h].float().numpy().astype(np.float64)
+        vh = v[b, h].float().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.dense_forward(qh, kh, vh, w.scale, w.window)
+        if with_bwd:
+            oracle.dense_backward(qh, kh, vh, do[b, h].float().numpy().astype(np.float64), w.scale, w.window)
+        t_total += time.perf_counter() - t0
+        done_f += flops_head_f * (3.5 if with_bwd else 1.0)
+        heads += 1
+        if t_total >= budget_s:
+            break
+    return done_f, t_total, heads
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    import torch
+
+    from exact_tiled_attention_02_gb300 import configs, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = configs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        run_reference(args, w, world)
+        return 0
+
+    from exact_tiled_attention_02_gb300 import binding as fa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    with_bwd = not args.no_bwd
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    dqd, dkd, dvd = (torch.empty_like(qd) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+
+    # does this build have the backward?
+    if with_bwd:
+        try:
+            fa.fa_bwd(qd, kd, vd, *fa.fa_fwd(qd, kd, vd, scale=w.scale, window=w.window), dod, scale=w.scale,
+                      window=w.window, dq=dqd, dk=dkd, dv=dvd, workspace=ws)
+        except fa.FaError as e:
+            if e.status != fa.FA_ERR_UNSUPPORTED:
+                raise
+            with_bwd = False
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fa_fwd(qd, kd, vd, scale=w.scale, window=w.window, o=od, lse=lsed)
+        if evs is not None:
+            evs[1].record(stream)
+        if with_bwd:
+            fa.fa_bwd(qd, kd, vd, od, lsed, dod, scale=w.scale, window=w.window, dq=dqd, dk=dkd, dv=dvd,
+                      workspace=ws)
+            if evs is not None:
+                evs[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if pg is not None:
+        pg.barrier()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if with_bwd else None
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert fa.fa_last_device_status() == fa.FA_OK, "a device-side wait timed out during the bench"
+
+    ms_per_step = total_ms / K
+    flops_fwd = w.fwd_flops()
+    flops_bwd = w.bwd_flops() if with_bwd else 0.0
+    flops_step = flops_fwd + flops_bwd
+    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    kernels = {"fwd": {"ms": fwd_ms, "tflops": flops_fwd / (fwd_ms * 1e-3) / 1e12}}
+    kernels["fwd"]["frac"] = kernels["fwd"]["tflops"] / peak
+    if with_bwd:
+        kernels["bwd"] = {"ms": bwd_ms, "tflops": flops_bwd / (bwd_ms * 1e-3) / 1e12}
+        kernels["bwd"]["frac"] = kernels["bwd"]["tflops"] / peak
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    src_file = {"fwd": "fwd_bf16_sm103.cu", "bwd": "bwd_bf16_sm103.cu"}[dom]
+    traffic = ncu_traffic(f"{dom}_bf16_sm103_{w.name}.md", src_file)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(kernels[dom]["tflops"], 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
+                "traffic": traffic, "peak_source": f"{peak_src} bf16 dense (burst)"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(fa, w, q, k, v, do, with_bwd, dev, min(K, 10), pg)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, secs, heads = oracle_sample(w, q, k, v, do, with_bwd, budget_s=10.0)
+        cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} heads, float64 numpy oracle "
+                         f"({'forward + backward' if with_bwd else 'forward'}), {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "attention TFLOP/s (fwd 4*B*H*N^2*d" + (" + bwd 2.5x" if with_bwd else "") + ")",
+            "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded standard normals, Q,K x8)",
+            "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
+                       "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (Q,K,V,O 4 x {:.0f} MB > 129 MB); no flush".format(
+                           qd.numel() * 2 / 1e6)},
+            "kernels": {n: {kk: round(vv, 4) for kk, vv in d.items()} for n, d in kernels.items()},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": K * (1 + (3 if with_bwd else 0)),
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg):
+    """Same metric through the public API with pinned host buffers: each step
+    copies the step's inputs host->device, runs the pass(es) and copies the
+    results back, all inside the timed region."""
+    import torch
+
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    dq_, dk_, dv_, ddo = (torch.empty_like(t, device=dev) for t in (q, k, v, do))
+    ho = torch.empty_like(q).pin_memory()
+    hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    hg = [torch.empty_like(q).pin_memory() for _ in range(3)]
+    od = torch.empty_like(dq_)
+    ld = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    gd = [torch.empty_like(dq_) for _ in range(3)]
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq_, dk_, dv_, scale=w.scale, window=w.window, o=od, lse=ld)
+        if with_bwd:
+            ddo.copy_(hdo, non_blocking=True)
+            fa.fa_bwd(dq_, dk_, dv_, od, ld, ddo, scale=w.scale, window=w.window, dq=gd[0], dk=gd[1], dv=gd[2],
+                      workspace=ws)
+            for h, g in zip(hg, gd):
+                h.copy_(g, non_blocking=True)
+        ho.copy_(od, non_blocking=True)
+        hl.copy_(ld, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    flops = w.fwd_flops() + (w.bwd_flops() if with_bwd else 0.0)
+    elem = q.numel() * q.element_size()
+    h2d = 3 * elem + (elem if with_bwd else 0)
+    d2h = elem + w.B * w.H * w.N * 4 + (3 * elem if with_bwd else 0)
+    return {"value": round(flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_reference(args, w, world):
+    """The oracle as it stands, timed on the host cores: each step is a
+    bounded sample (one head) of the same workload."""
+    from exact_tiled_attention_02_gb300 import inputs
+
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    with_bwd = not args.no_bwd
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, do, with_bwd, budget_s=0.0, max_heads=1)
+    fl_tot, t_tot = 0.0, 0.0
+    for _ in range(args.steps):
+        fl, secs, _ = oracle_sample(w, q, k, v, do, with_bwd, budget_s=0.0, max_heads=1)
+        fl_tot += fl
+        t_tot += secs
+    value = fl_tot / t_tot / 1e12
+    cores = cpu_cores()
+    line = {
+        "metric": "attention TFLOP/s (fwd 4*B*H*N^2*d" + (" + bwd 2.5x" if with_bwd else "") + ")",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded standard normals, Q,K x8)", "impl": "reference",
+        "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
+                   "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one head per step (head 0,0), float64 numpy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,73 @@
+// kernels.h -- internal interface between the C-ABI layer (fa_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Arguments shared by every forward kernel.  Arrays are [B,H,N,d] row-major;
+// lse is [B,H,N].  window_r < 0 means unmasked.
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;  // may be null
+  int BH;      // B * H
+  int N;
+  int d;
+  int window_r;
+  float scale;       // multiplies raw scores
+  float scale_log2;  // scale * log2(e)
+  unsigned int* status;
+  unsigned long long wait_ns;
+};
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;  // [B,H,N,d] fp32 workspace
+  float* dsum;    // [B,H,N]   fp32 workspace: D_i = sum_k dO_ik O_ik
+  int BH;
+  int N;
+  int d;
+  int window_r;
+  float scale;
+  float scale_log2;
+  unsigned int* status;
+  unsigned long long wait_ns;
+};
+
+// 3-D TMA maps over a [BH, N, d] bf16 array: dims (d, N, BH), box
+// (64, rows, 1), 128-byte swizzle, zero fill out of bounds.
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+struct BwdMaps {
+  CUtensorMap q, k, v, dO;
+};
+
+// Launchers (each returns the launch's cudaError_t).
+cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
+cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, cudaStream_t s);
+
+// Row counts of the tiles the TMA boxes use (host needs them for the maps).
+constexpr int kFwdBlockRows = 128;  // query rows per CTA tile
+constexpr int kFwdBlockCols = 128;  // keys per K/V tile
+constexpr int kBwdBlockRows = 128;  // query rows per step of the backward
+constexpr int kBwdBlockCols = 128;  // keys per CTA of the backward
+
+}  // namespace fa

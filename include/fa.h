@@ -1,0 +1,143 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention library (libfa.so) for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The operation is exact scaled-dot-product attention, per (batch, head):
+ *
+ *     S = Q K^T * scale,   P = softmax_row(S),   O = P V,
+ *     lse_i = ln sum_j exp(S_ij)
+ *
+ * as stated in "Flash attention and efficient attention -- Hinglish notes",
+ * section "The Standard Attention Problem" (the page's "S / d_k" reads as
+ * S / sqrt(d_k): its worked example's 0.707 for d = 2 needs the square root),
+ * computed one tile at a time with running max / running sum statistics as in
+ * that page's "Derivation: Incremental Softmax" (Steps 1-3) and in "Compute
+ * attention one tile at a time" (TensorViz), step "tiles", so the N x N score
+ * matrix never reaches device memory.  The optional local window follows the
+ * notes' "Worked example Local Attention Window": query i attends to key j
+ * iff |i - j| <= (window - 1) / 2.  The backward pass recomputes S and P on
+ * chip from Q, K, V, O, dO and the saved lse ("Backward Pass: Recomputation").
+ *
+ * Common conventions for every entry point
+ * ----------------------------------------
+ * Layout     Q, K, V, O, dO, dQ, dK, dV are dense, contiguous, row-major
+ *            [B, H, N, d] arrays in device memory; lse (and the backward's D)
+ *            are [B, H, N] float32.  Every base pointer must be 16-byte aligned.
+ * dtype      FA_DTYPE_BF16: Q/K/V/O/dO/dQ/dK/dV are bfloat16, arithmetic is
+ *            fp32-accumulated tensor-core math with P rounded to bf16 before
+ *            the P V product; d must be 64 or 128.
+ *            FA_DTYPE_F32: all arrays are float32 and all arithmetic is exact
+ *            fp32 on CUDA cores; 1 <= d <= 128 (forward only in this version).
+ * scale      finite and > 0; usually 1/sqrt(d).
+ * window     <= 0: unmasked.  Otherwise an odd full width w; r = (w - 1) / 2.
+ *            Even widths are rejected (the pages give them no meaning).
+ * stream     a cudaStream_t passed as void*; NULL is the legacy default
+ *            stream.  All work is enqueued on it; no call synchronises except
+ *            fa_last_device_status().
+ * Ownership  the caller owns every buffer.  The library allocates no device
+ *            memory and keeps no pointer after a call returns.
+ * Errors     argument errors are detected on the host before anything is
+ *            launched and return FA_ERR_INVALID or FA_ERR_UNSUPPORTED with no
+ *            side effect.  A failed launch returns FA_ERR_CUDA.  Every wait
+ *            inside the kernels is bounded in time; a wait that runs out
+ *            records FA_ERR_TIMEOUT in the library's device status word and
+ *            the kernel returns early (its outputs are then undefined), which
+ *            fa_last_device_status() reports.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,      /* bad pointer, size, alignment, scale or window */
+  FA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (dtype/d) */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out */
+} fa_status;
+
+typedef enum { FA_DTYPE_F32 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
+
+/*
+ * Forward pass: O = softmax(Q K^T * scale) V, and lse.
+ *   q, k, v  [B,H,N,d] inputs (read only).
+ *   o        [B,H,N,d] output, same dtype as the inputs.
+ *   lse      [B,H,N] float32 output (natural log of the row sum of exp over
+ *            the scaled, masked scores), or NULL if not wanted.
+ * Sources: the notes' "The Standard Attention Problem" (what is computed),
+ * "Derivation: Incremental Softmax" Steps 1-3 and TensorViz step "tiles" (how:
+ * running max m, running sum l, rescale when m rises, divide by l at the end),
+ * "Worked example Local Attention Window" (window; key tiles wholly outside
+ * the band are never loaded).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int window, fa_dtype dt,
+                 void* stream);
+
+/*
+ * Size in bytes of the workspace fa_bwd needs for a problem of this shape:
+ * a float32 [B,H,N,d] dQ accumulator followed by a float32 [B,H,N] array of
+ * D_i = sum_j dO_ij O_ij, each section 256-byte aligned.  Returns 0 for
+ * non-positive sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation: given Q, K, V, the forward output O, its
+ * lse and the output gradient dO, writes dQ, dK, dV (same dtype and layout
+ * as Q).  S and P are rebuilt on chip from Q, K and lse; nothing of size
+ * N x N is read or written.  Sources: the notes' "Backward Pass:
+ * Recomputation" (recompute, do not store, S and P); the gradient formulas
+ * are the derivative of the forward definition (the pages print none):
+ * dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij = sum_k dO_ik O_ik,
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ *   workspace        device scratch of at least fa_bwd_workspace_bytes(),
+ *                    owned by the caller, 256-byte aligned; its contents on
+ *                    entry do not matter and are undefined on return.
+ *   workspace_bytes  its size; smaller than required -> FA_ERR_INVALID.
+ * bf16, d = 128 (and d = 64) only in this version; FA_DTYPE_F32 returns
+ * FA_ERR_UNSUPPORTED.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale, int window, fa_dtype dt,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream` (as void* cudaStream_t), then reads and clears the
+ * device status word that the kernels set when a bounded wait runs out.
+ * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if synchronising failed.
+ */
+fa_status fa_last_device_status(void* stream);
+
+/*
+ * Sets the time limit, in microseconds, of every device-side wait in kernels
+ * launched afterwards by this process (default 1,000,000 = 1 s; values <= 0
+ * restore the default).  Returns the previous limit.
+ */
+long long fa_set_wait_limit_us(long long limit_us);
+
+/*
+ * Self-test of the bounded wait: launches one block that waits on a shared
+ * memory barrier nothing ever arrives on, for `limit_us` microseconds
+ * (1..100000), then gives up, records FA_ERR_TIMEOUT in the status word and
+ * returns.  A caller checks fa_last_device_status() == FA_ERR_TIMEOUT.
+ */
+fa_status fa_selftest_wait_timeout(int limit_us, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,191 @@
+"""GPU parity of the forward pass against the float64 oracle, through the C ABI.
+
+Tolerances: fp32 max-abs 1e-5; bf16 O max-abs 2e-2 and mean-abs 2e-3; lse
+(both dtypes) |diff| <= 1e-3 + 1e-5 |lse| for bf16, 1e-5 for fp32.  Small and
+medium shapes are compared element by element (several tiles and a ragged
+tail); the full-size workloads are compared on sampled rows that the oracle
+computes one by one, plus properties that hold at any size.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_02_gb300 import configs, inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _fa():
+    from exact_tiled_attention_02_gb300 import binding
+    return binding
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _check_bf16(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    err = np.abs(_np(o_gpu) - o_ref)
+    assert np.all(np.isfinite(_np(o_gpu))), what
+    assert err.max() <= 2e-2, (what, err.max())
+    assert err.mean() <= 2e-3, (what, err.mean())
+    if lse_gpu is not None:
+        le = np.abs(_np(lse_gpu) - lse_ref)
+        assert np.all(le <= 1e-3 + 1e-5 * np.abs(lse_ref)), (what, le.max())
+
+
+def test_workload1_f32_exact():
+    dev = _dev()
+    w = configs.WORKLOADS[1]
+    q, k, v = inputs.workload_inputs(w)
+    o, lse = _fa().fa_fwd(q.to(dev), k.to(dev), v.to(dev), scale=w.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.dense_forward(_np(q), _np(k), _np(v), w.scale)
+    assert np.abs(_np(o) - o_ref).max() <= 1e-5
+    assert np.abs(_np(lse) - lse_ref).max() <= 1e-5
+    assert _fa().fa_last_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,N,d,window", [
+    (1, 1, 1, 1, 0), (1, 2, 5, 4, 0), (2, 1, 33, 17, 0), (1, 3, 100, 64, 0), (1, 1, 77, 128, 0),
+    (1, 2, 50, 8, 3), (1, 1, 200, 32, 65), (2, 2, 129, 4, 257),
+])
+def test_f32_shapes(B, H, N, d, window):
+    dev = _dev()
+    q, k, v = inputs.make_inputs(B, H, N, d, "f32", seed=N + d)
+    o, lse = _fa().fa_fwd(q.to(dev), k.to(dev), v.to(dev), window=window)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.dense_forward(_np(q), _np(k), _np(v), 1 / np.sqrt(d), window)
+    assert np.abs(_np(o) - o_ref).max() <= 1e-5
+    assert np.abs(_np(lse) - lse_ref).max() <= 1e-5
+
+
+BF16_CASES = [
+    # B, H, N, d, window, qk_mult
+    (1, 1, 1, 64, 0, 1.0),
+    (1, 2, 7, 128, 0, 1.0),
+    (1, 2, 128, 64, 0, 1.0),
+    (2, 1, 129, 128, 0, 1.0),
+    (1, 3, 300, 64, 0, 1.0),
+    (1, 2, 513, 128, 0, 1.0),
+    (1, 1, 1000, 128, 0, 8.0),
+    (2, 2, 384, 64, 0, 8.0),
+    (1, 2, 300, 128, 3, 1.0),
+    (1, 1, 700, 128, 65, 1.0),
+    (1, 2, 1000, 64, 257, 1.0),
+    (1, 1, 640, 128, 257, 8.0),
+    (1, 1, 257, 128, 513, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,window,qk", BF16_CASES)
+def test_bf16_elementwise(B, H, N, d, window, qk):
+    dev = _dev()
+    q, k, v = inputs.make_inputs(B, H, N, d, "bf16", seed=N * 7 + d + window, qk_mult=qk)
+    o, lse = _fa().fa_fwd(q.to(dev), k.to(dev), v.to(dev), window=window)
+    torch.cuda.synchronize()
+    assert _fa().fa_last_device_status() == 0
+    o_ref, lse_ref = oracle.dense_forward(_np(q), _np(k), _np(v), 1 / np.sqrt(d), window)
+    _check_bf16(o, lse, o_ref, lse_ref, (B, H, N, d, window, qk))
+
+
+def test_bf16_deterministic_and_no_lse():
+    dev = _dev()
+    q, k, v = (t.to(dev) for t in inputs.make_inputs(2, 2, 333, 128, "bf16", seed=5))
+    o1, l1 = _fa().fa_fwd(q, k, v)
+    o2, l2 = _fa().fa_fwd(q, k, v)
+    o3, l3 = _fa().fa_fwd(q, k, v, want_lse=False)
+    torch.cuda.synchronize()
+    assert l3 is None
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+def test_bf16_guard_bands():
+    """Outputs are written exactly inside [B,H,N,d] / [B,H,N]: canaries around
+    them stay untouched for a ragged N."""
+    dev = _dev()
+    B, H, N, d = 1, 3, 200, 128
+    q, k, v = (t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=9))
+    pad = 4096
+    obuf = torch.full((2 * pad + B * H * N * d,), 7.0, device=dev, dtype=torch.bfloat16)
+    lbuf = torch.full((2 * pad + B * H * N,), -3.0, device=dev, dtype=torch.float32)
+    o = obuf[pad:pad + B * H * N * d].view(B, H, N, d)
+    lse = lbuf[pad:pad + B * H * N].view(B, H, N)
+    _fa().fa_fwd(q, k, v, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(obuf[:pad] == 7.0) and torch.all(obuf[-pad:] == 7.0)
+    assert torch.all(lbuf[:pad] == -3.0) and torch.all(lbuf[-pad:] == -3.0)
+    o_ref, lse_ref = oracle.dense_forward(_np(q), _np(k), _np(v), 1 / np.sqrt(d))
+    _check_bf16(o, lse, o_ref, lse_ref)
+
+
+def _sample_rows(N, rng, extra=24):
+    fixed = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1}
+    rows = sorted({r for r in fixed if 0 <= r < N} | set(rng.integers(0, N, extra).tolist()))
+    return np.array(rows)
+
+
+@pytest.mark.parametrize("index", [2, 3, 4])
+def test_full_size_workloads_sampled(index):
+    """The full-size forward workloads, launched exactly as the bench launches
+    them, compared on sampled rows of sampled heads; plus finiteness and the
+    convex-hull property on every output."""
+    dev = _dev()
+    w = configs.WORKLOADS[index]
+    q, k, v = inputs.workload_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = _fa().fa_fwd(qd, kd, vd, scale=w.scale, window=w.window)
+    torch.cuda.synchronize()
+    assert _fa().fa_last_device_status() == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    vmax = vd.float().amax(dim=2, keepdim=True)
+    vmin = vd.float().amin(dim=2, keepdim=True)
+    assert bool(((o.float() <= vmax + 1e-2) & (o.float() >= vmin - 1e-2)).all())
+    rng = np.random.default_rng(index)
+    heads = [(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))]
+    for b, h in heads:
+        rows = _sample_rows(w.N, rng)
+        o_ref, lse_ref = oracle.dense_forward_rows(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), w.scale, rows,
+                                                   window=w.window)
+        _check_bf16(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, (index, b, h))
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    dev = _dev()
+    fa = _fa()
+    assert fa.fa_last_device_status() == 0
+    assert fa.fa_selftest_wait_timeout(2000) == 0
+    assert fa.fa_last_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_last_device_status() == 0  # cleared by the read
+    # the context is still usable
+    q, k, v = (t.to(dev) for t in inputs.make_inputs(1, 1, 130, 64, "bf16", seed=1))
+    o, lse = fa.fa_fwd(q, k, v)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.dense_forward(_np(q), _np(k), _np(v), 0.125)
+    _check_bf16(o, lse, o_ref, lse_ref)
+    assert fa.fa_last_device_status() == 0
+
+
+def test_binding_rejects_bad_tensors():
+    dev = _dev()
+    fa = _fa()
+    q = torch.zeros(1, 1, 8, 64, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q.float())
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q.transpose(2, 3).contiguous().transpose(2, 3))
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd(q, q, q, window=4)
+    x = torch.zeros(1, 1, 8, 96, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd(x, x, x)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
