@@ -156,10 +156,9 @@ long long fa_set_wait_limit_us(long long limit_us) {
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  const size_t acc = (rows * d * sizeof(float) + 255) & ~size_t(255);
-  const size_t dsum = (rows * sizeof(float) + 255) & ~size_t(255);
-  return acc + dsum;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL) return 0;
+  return bwd_workspace_layout(static_cast<int>(bh), N, d, nullptr, nullptr);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -218,9 +217,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  const size_t rows = static_cast<size_t>(B) * H * N;
+  size_t off_lse2 = 0, off_dsum = 0;
+  bwd_workspace_layout(B * H, N, d, &off_lse2, &off_dsum);
   p.dq_acc = static_cast<float*>(workspace);
-  p.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * sizeof(float) + 255) & ~size_t(255)));
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_lse2);
+  p.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_dsum);
   p.BH = B * H;
   p.N = N;
   p.d = d;

@@ -21,8 +21,8 @@
  * Common conventions for every entry point
  * ----------------------------------------
  * Layout     Q, K, V, O, dO, dQ, dK, dV are dense, contiguous, row-major
- *            [B, H, N, d] arrays in device memory; lse (and the backward's D)
- *            are [B, H, N] float32.  Every base pointer must be 16-byte aligned.
+ *            [B, H, N, d] arrays in device memory; lse is [B, H, N] float32.
+ *            Every base pointer must be 16-byte aligned.
  * dtype      FA_DTYPE_BF16: Q/K/V/O/dO/dQ/dK/dV are bfloat16, arithmetic is
  *            fp32-accumulated tensor-core math with P rounded to bf16 before
  *            the P V product; d must be 64 or 128.
@@ -81,8 +81,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Size in bytes of the workspace fa_bwd needs for a problem of this shape:
- * a float32 [B,H,N,d] dQ accumulator followed by a float32 [B,H,N] array of
- * D_i = sum_j dO_ij O_ij, each section 256-byte aligned.  Returns 0 for
+ * a float32 [B,H,N,d] dQ accumulator, then two float32 [B,H,Npad] arrays
+ * (lse_i * log2(e) and D_i = sum_k dO_ik O_ik; Npad = N rounded up to a
+ * multiple of 64), each section 256-byte aligned.  Returns 0 for
  * non-positive sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
@@ -100,7 +101,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                    owned by the caller, 256-byte aligned; its contents on
  *                    entry do not matter and are undefined on return.
  *   workspace_bytes  its size; smaller than required -> FA_ERR_INVALID.
- * bf16, d = 128 (and d = 64) only in this version; FA_DTYPE_F32 returns
+ * bf16 with d = 128 only in this version; other d and FA_DTYPE_F32 return
  * FA_ERR_UNSUPPORTED.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

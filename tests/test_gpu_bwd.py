@@ -1,0 +1,133 @@
+"""GPU parity of the backward pass (recomputation) against the float64 oracle's
+analytic gradients, through the C ABI.
+
+The forward's O and lse come from the library's own forward (as in training);
+the oracle differentiates the definition from Q, K, V and dO alone.  Bar:
+relative L2 error <= 1e-2 for each of dQ, dK, dV.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_02_gb300 import configs, inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _fa():
+    from exact_tiled_attention_02_gb300 import binding
+    return binding
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _check_grad(name, g, r, what):
+    """Relative L2 <= 1e-2; where the exact gradient is identically zero (one
+    key: every softmax row is [1], so dS = 0 and dQ = dK = 0) a relative error
+    is undefined and the bar is an absolute 1e-5 instead."""
+    assert np.all(np.isfinite(g)), (name, what)
+    if np.linalg.norm(r) == 0.0:
+        assert np.max(np.abs(g)) <= 1e-5, (name, np.max(np.abs(g)), what)
+    else:
+        assert _rel(g, r) <= 1e-2, (name, _rel(g, r), what)
+
+
+def _run(q, k, v, do, scale, window, dev):
+    fa = _fa()
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd(qd, kd, vd, scale=scale, window=window)
+    dq, dk, dv = fa.fa_bwd(qd, kd, vd, o, lse, dod, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    return dq, dk, dv
+
+
+BWD_CASES = [
+    # B, H, N, d, window, qk_mult
+    (1, 1, 1, 128, 0, 1.0),
+    (1, 2, 5, 128, 0, 1.0),
+    (1, 1, 64, 128, 0, 1.0),
+    (1, 2, 65, 128, 0, 1.0),
+    (2, 1, 200, 128, 0, 1.0),
+    (1, 2, 300, 128, 0, 8.0),
+    (1, 1, 513, 128, 0, 1.0),
+    (1, 2, 300, 128, 3, 1.0),
+    (1, 1, 700, 128, 65, 1.0),
+    (1, 1, 1000, 128, 257, 1.0),
+    (1, 1, 640, 128, 257, 8.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,window,qk", BWD_CASES)
+def test_bwd_elementwise(B, H, N, d, window, qk):
+    dev = _dev()
+    q, k, v, do = inputs.make_inputs(B, H, N, d, "bf16", seed=3 * N + window, qk_mult=qk, with_do=True)
+    scale = 1 / np.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, scale, window, dev)
+    refs = oracle.dense_backward(_np(q), _np(k), _np(v), _np(do), scale, window)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        _check_grad(name, _np(g), r, (B, H, N, d, window, qk))
+
+
+def test_bwd_deterministic_dk_dv():
+    """dK and dV are reduced on chip without atomics, so they are bitwise
+    repeatable; dQ (fp32 atomics) is repeatable to rounding."""
+    dev = _dev()
+    q, k, v, do = inputs.make_inputs(1, 2, 333, 128, "bf16", seed=4, with_do=True)
+    a = _run(q, k, v, do, 1 / np.sqrt(128), 0, dev)
+    b = _run(q, k, v, do, 1 / np.sqrt(128), 0, dev)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert _rel(_np(a[0]), _np(b[0])) <= 1e-3
+
+
+def test_workload5_full_size_sampled_heads():
+    """The full-size backward workload, launched as the bench launches it:
+    three whole heads against the oracle, plus identities of the exact
+    gradient over every head."""
+    dev = _dev()
+    w = configs.WORKLOADS[5]
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    dq, dk, dv = _run(q, k, v, do, w.scale, w.window, dev)
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g.float()).all()
+    rng = np.random.default_rng(5)
+    heads = [(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))]
+    for b, h in heads:
+        refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), w.scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
+            assert _rel(_np(g), r) <= 1e-2, (name, b, h, _rel(_np(g), r))
+    # sum over keys of dK vanishes; sum over keys of dV equals the sum over queries of dO
+    sk = dk.float().sum(dim=2)
+    assert float(sk.abs().max()) <= 2e-2 * float(dk.float().abs().sum(dim=2).max())
+    sv = dv.float().sum(dim=2)
+    sdo = do.to(dev).float().sum(dim=2)
+    assert float((sv - sdo).norm() / sdo.norm()) <= 1e-2
+
+
+def test_bwd_unsupported_requests():
+    dev = _dev()
+    fa = _fa()
+    x = torch.zeros(1, 1, 8, 64, device=dev, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 1, 8, device=dev, dtype=torch.float32)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(x, x, x, x, lse, x)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+    y = torch.zeros(1, 1, 8, 128, device=dev, dtype=torch.float32)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(y, y, y, y, lse, y)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
