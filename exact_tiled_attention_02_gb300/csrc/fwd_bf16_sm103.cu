@@ -12,20 +12,28 @@
 // time" (TensorViz), step "tiles": the maximum and denominator of each query
 // row are carried across tiles, earlier contributions are rescaled when the
 // maximum rises, and the numerator is divided by the denominator once, at the
-// end.  The score tile lives only in tensor memory; nothing of size N x N
-// reaches device memory.
+// end.  Score tiles live only in tensor memory; nothing of size N x N reaches
+// device memory.
 //
-// CTA = one 128-row query tile of one (batch, head); 192 threads:
-//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t)
-//   warp  4    TMA producer (one elected lane)
-//   warp  5    TMEM owner + tcgen05.mma issuer (one elected lane)
-// Tensor memory (512 columns x 128 lanes, fp32):
-//   cols [0,128) S buffer 0, [128,256) S buffer 1, [256,256+D) O accumulator.
-// Shared memory (1024-byte aligned, all operands 128-byte swizzled):
-//   Q tile, STAGES x K tile, STAGES x V tile, P tile (bf16), barriers.
-// Per key tile j the MMA warp issues S_{j+1} = Q K_{j+1}^T before O += P_j V_j,
-// so the tensor core computes the next scores while the softmax warps work
-// on the current ones.
+// CTA = two 128-row query tiles (Q0, Q1) of one (batch, head); 384 threads:
+//   warps 0-3  softmax for Q0: thread t owns row t of Q0 (TMEM lane t)
+//   warps 4-7  softmax for Q1: thread t owns row t of Q1 (TMEM lane t)
+//   warp  8    TMEM owner + tcgen05.mma issuer (one elected lane)
+//   warp  9    TMA producer (one elected lane)
+//   warps 10-11 idle (registers are granted per warpgroup of four warps, so
+//              a ten-warp CTA costs as much as twelve; 168 per thread)
+// Tensor memory (512 columns x 128 lanes, 32-bit):
+//   [0,128) S0 (P0 as packed bf16 in its first 64 columns), [128,256) S1 / P1,
+//   [256,256+D) O0, [384,384+D) O1.
+// Shared memory (1024-byte aligned, 128-byte swizzled): Q0, Q1, a ring of
+// STAGES K/V tiles, barriers.
+// The two query tiles ping-pong: while the softmax warps of one tile turn
+// S into P, the tensor core runs the other tile's P V and Q K^T, so the
+// exponentials of one tile overlap the matrix products of the other.  Per key
+// tile j the MMA warp issues  O0 += P0 V_j,  S0 = Q0 K_{j+1}^T,  O1 += P1 V_j,
+// S1 = Q1 K_{j+1}^T; tcgen05.mma operations issued by one thread execute in
+// order, so S_i(j+1) overwrites the columns of P_i(j) only after P_i(j) V_j
+// has read them.
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -34,44 +42,68 @@ namespace {
 
 using namespace sm103;
 
-constexpr int BR = kFwdBlockRows;
-constexpr int BC = kFwdBlockCols;
-constexpr int kThreads = 192;
+constexpr int BR = kFwdBlockRows;  // rows per query tile (two per CTA)
+constexpr int BC = kFwdBlockCols;  // keys per K/V tile
+constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 256;
-// Lazy rescaling: the reference maximum of a row is raised only when a new
-// score exceeds it by more than 2^8 in linear terms.  The final O / l uses
-// the same reference for numerator and denominator, so the result is the
-// same exact quantity; P stays <= 256 (bf16 and fp32 hold that easily).
+constexpr uint32_t kTmemS = 0;    // + 128 * tile
+constexpr uint32_t kTmemO = 256;  // + 128 * tile
+// Lazy rescaling: a row's reference maximum is raised only when a new score
+// exceeds it by more than 2^8 in linear terms.  The final O / l uses the same
+// reference for numerator and denominator, so the result is the same exact
+// quantity; P stays <= 256 (bf16 and fp32 hold that easily).
 constexpr float kRescaleThreshold = 8.0f;
+
+// 2^x on the FMA pipe, for the share of exponentials the special-function
+// unit does not take: Cody-Waite style range reduction x = n + f with
+// n = round(x) (by the 1.5 * 2^23 rounding constant), f in [-1/2, 1/2];
+// 2^f by a degree-3 polynomial (our own minimax fit for relative error,
+// max 7.5e-5, from csrc/fit_exp2_poly.py); 2^n by adding n to the exponent
+// field.  x is clamped at -126, so results never underflow to denormals; the
+// kernel uses this only where no score is masked.
+__device__ __forceinline__ float exp2_poly(float x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f, c2 = 0.2426111251115799f,
+                  c3 = 0.0551716685295105f;
+  x = fmaxf(x, -126.0f);
+  const float t = __fadd_rn(x, kRound);
+  const float n = __fadd_rn(t, -kRound);
+  const float f = __fadd_rn(x, -n);
+  float p = fmaf(c3, f, c2);
+  p = fmaf(p, f, c1);
+  p = fmaf(p, f, c0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
 
 template <int D>
 struct Cfg {
   static constexpr int STAGES = (D == 128) ? 2 : 3;
   static constexpr int BOXES = D / 64;         // 64-column (128-byte) boxes per row
-  static constexpr int Q_BYTES = BR * D * 2;
+  static constexpr int Q_BYTES = BR * D * 2;   // one query tile
   static constexpr int KV_BYTES = BC * D * 2;  // one K or one V tile
-  static constexpr int P_BYTES = BR * BC * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], s_free[2], p_full, pv_done, drain
-  static constexpr int NBAR = 1 + 3 * STAGES + 2 + 2 + 3;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  // q_full[2], k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 2 + 3 * STAGES + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(kTmemO + D <= kTmemCols, "tensor memory budget");
+  static_assert(D <= 128, "tensor memory budget");
 };
 
+template <int STAGES>
 struct Bars {
-  uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, s_free0, p_full, pv_done, drain;
-  __device__ uint32_t k_full(int s) const { return k_full0 + 8 * s; }
-  __device__ uint32_t v_full(int s) const { return v_full0 + 8 * s; }
-  __device__ uint32_t kv_empty(int s) const { return kv_empty0 + 8 * s; }
-  __device__ uint32_t s_full(int b) const { return s_full0 + 8 * b; }
-  __device__ uint32_t s_free(int b) const { return s_free0 + 8 * b; }
+  uint32_t base;
+  __device__ uint32_t q_full(int t) const { return base + 8 * t; }
+  __device__ uint32_t k_full(int s) const { return base + 8 * (2 + s); }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (2 + STAGES + s); }
+  __device__ uint32_t kv_empty(int s) const { return base + 8 * (2 + 2 * STAGES + s); }
+  __device__ uint32_t s_full(int t) const { return base + 8 * (2 + 3 * STAGES + t); }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (4 + 3 * STAGES + t); }
+  __device__ uint32_t o_done(int t) const { return base + 8 * (6 + 3 * STAGES + t); }
+  __device__ uint32_t drain() const { return base + 8 * (8 + 3 * STAGES); }
 };
 
 template <int D>
@@ -82,70 +114,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
-
-  Bars bar;
-  {
-    uint32_t b = sb + C::OFF_BAR;
-    bar.q_full = b;
-    b += 8;
-    bar.k_full0 = b;
-    b += 8 * C::STAGES;
-    bar.v_full0 = b;
-    b += 8 * C::STAGES;
-    bar.kv_empty0 = b;
-    b += 8 * C::STAGES;
-    bar.s_full0 = b;
-    b += 16;
-    bar.s_free0 = b;
-    b += 16;
-    bar.p_full = b;
-    b += 8;
-    bar.pv_done = b;
-    b += 8;
-    bar.drain = b;
-  }
+  const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
+  const Bars<C::STAGES> bar{sb + C::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const WaitCtl wc{p.status, abort_flag, p.wait_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nqt = (p.N + BR - 1) / BR;
-  const int bh = blockIdx.x / nqt;
-  const int i0 = (blockIdx.x % nqt) * BR;
   const int N = p.N;
   const int r = p.window_r;
+  const int nqt = (N + 2 * BR - 1) / (2 * BR);
+  const int bh = blockIdx.x / nqt;
+  const int i0 = (blockIdx.x % nqt) * (2 * BR);  // first row of Q0; Q1 starts at i0 + BR
 
-  // key tiles this query tile needs (only in-band tiles when windowed)
+  // key tiles the two query tiles need (only in-band tiles when windowed)
   int j_lo = 0, j_hi = (N + BC - 1) / BC;
   if (r >= 0) {
     const int lo = max(0, i0 - r);
-    const int hi = min(N, i0 + BR + r);  // exclusive
+    const int hi = min(N, i0 + 2 * BR + r);  // exclusive
     j_lo = lo / BC;
     j_hi = (hi + BC - 1) / BC;
   }
   const int ntiles = j_hi - j_lo;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar.q_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.s_full(t), 1);
+      mbar_init(bar.p_full(t), 4);  // one arrive per softmax warp of the tile
+      mbar_init(bar.o_done(t), 1);
+    }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar.k_full(s), 1);
       mbar_init(bar.v_full(s), 1);
       mbar_init(bar.kv_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar.s_full(b), 1);
-      mbar_init(bar.s_free(b), 4);  // one arrive per softmax warp
-    }
-    mbar_init(bar.p_full, 4);
-    mbar_init(bar.pv_done, 1);
-    mbar_init(bar.drain, 1);
+    mbar_init(bar.drain(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 5) {
+  if (warp == 8) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -154,15 +164,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp >= 10) {
+    // idle warps of the third warpgroup
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       prefetch_tensormap(&tmq);
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
-      mbar_arrive_expect_tx(bar.q_full, C::Q_BYTES);
+      for (int t = 0; t < 2; ++t) {
+        mbar_arrive_expect_tx(bar.q_full(t), C::Q_BYTES);
 #pragma unroll
-      for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sQ + b * BR * 128, &tmq, bar.q_full, b * 64, i0, bh);
+        for (int b = 0; b < C::BOXES; ++b)
+          tma_load_3d(sQ + t * C::Q_BYTES + b * BR * 128, &tmq, bar.q_full(t), b * 64, i0 + t * BR, bh);
+      }
       int issued = 0;
       for (int it = 0; it < ntiles; ++it) {
         const int st = it % C::STAGES;
@@ -182,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory is released
         WaitCtl drain{nullptr, nullptr, wc.limit_ns};
-        mbar_wait(bar.q_full, 0, drain);
+        mbar_wait(bar.q_full(0), 0, drain);
+        mbar_wait(bar.q_full(1), 0, drain);
         for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
           const int st = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -192,60 +208,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BR, BC, 0, 0);  // Q: K-major, K tile: K-major
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, D, 0, 1);   // P: K-major, V tile: MN-major
-      bool ok = mbar_wait(bar.q_full, 0, wc);
-      auto issue_qk = [&](int it) -> bool {
-        const int st = it % C::STAGES;
-        const uint32_t ph = (it / C::STAGES) & 1;
-        const int b = it & 1;
-        if (!mbar_wait(bar.k_full(st), ph, wc)) return false;
-        if (!mbar_wait(bar.s_free(b), ((it >> 1) & 1) ^ 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t kbase = sK + st * C::KV_BYTES;
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, D, 0, 1);   // P (TMEM), V tile: MN-major
+      auto issue_s = [&](int t, int it) {  // S_t = Q_t K_it^T
+        const uint32_t kbase = sK + (it % C::STAGES) * C::KV_BYTES;
+        const uint32_t qbase = sQ + t * C::Q_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
+          const uint32_t offq = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
           const uint32_t offk = (kk >> 2) * (BC * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + b * BC, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + offk, 16, 1024),
-                      idesc_qk, kk > 0);
+          mma_bf16_ss(tmem + kTmemS + t * 128, sdesc_sw128(qbase + offq, 16, 1024),
+                      sdesc_sw128(kbase + offk, 16, 1024), idesc_qk, kk > 0);
         }
-        mma_commit(bar.s_full(b));
-        return true;
+        mma_commit(bar.s_full(t));
       };
-      if (ok) ok = issue_qk(0);
+      auto issue_pv = [&](int t, int it) {  // O_t += P_t V_it
+        const uint32_t vbase = sV + (it % C::STAGES) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_bf16_ts(tmem + kTmemO + t * 128, tmem + kTmemS + t * 128 + kk * 8,
+                      sdesc_sw128(vbase + kk * 16 * 128, BC * 128, 1024), idesc_pv, (it > 0 || kk > 0));
+        mma_commit(bar.o_done(t));
+      };
+      bool ok = mbar_wait(bar.q_full(0), 0, wc) && mbar_wait(bar.k_full(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        ok = mbar_wait(bar.q_full(1), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_s(1, 0);
+        }
+      }
       for (int it = 0; ok && it < ntiles; ++it) {
-        if (it + 1 < ntiles && !issue_qk(it + 1)) break;
         const int st = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1;
+        const bool more = it + 1 < ntiles;
         if (!mbar_wait(bar.v_full(st), ph, wc)) break;
-        if (!mbar_wait(bar.p_full, it & 1, wc)) break;
+        if (!mbar_wait(bar.p_full(0), it & 1, wc)) break;
         tc_fence_after();
-        const uint32_t vbase = sV + st * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk) {
-          const uint32_t offp = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kTmemO, sdesc_sw128(sP + offp, 16, 1024),
-                      sdesc_sw128(vbase + kk * 16 * 128, BC * 128, 1024), idesc_pv, (it > 0 || kk > 0));
+        issue_pv(0, it);
+        if (more) {
+          if (!mbar_wait(bar.k_full((it + 1) % C::STAGES), ((it + 1) / C::STAGES) & 1, wc)) break;
+          tc_fence_after();
+          issue_s(0, it + 1);
         }
+        if (!mbar_wait(bar.p_full(1), it & 1, wc)) break;
+        tc_fence_after();
+        issue_pv(1, it);
         mma_commit(bar.kv_empty(st));
-        mma_commit(bar.pv_done);
+        if (more) issue_s(1, it + 1);
       }
       // every MMA this thread issued must finish before tensor memory is freed
-      mma_commit(bar.drain);
+      mma_commit(bar.drain());
       WaitCtl drain{nullptr, nullptr, wc.limit_ns};
-      mbar_wait(bar.drain, 0, drain);
+      mbar_wait(bar.drain(), 0, drain);
     }
     __syncwarp();
   } else {
     // -------------------------------------------------------------- softmax
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int qi = i0 + row;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int t = warp >> 2;             // query tile of this warpgroup
+    const int row = threadIdx.x & 127;   // row within the tile == TMEM lane
+    const int qi = i0 + t * BR + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t tS = tl + kTmemS + t * 128, tO = tl + kTmemO + t * 128;
     const float sl = p.scale_log2;
+    const int qlo = i0 + t * BR, qhi = qlo + BR - 1;  // rows of this tile
     float m_ref = -INFINITY;  // running reference maximum, log2 units of scaled scores
     float l = 0.f;
     bool ok = true;
@@ -254,25 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
     };
     for (int it = 0; it < ntiles; ++it) {
-      const int b = it & 1;
-      if (!warp_wait(bar.s_full(b), (it >> 1) & 1)) {
+      if (!warp_wait(bar.s_full(t), it & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[BC];
 #pragma unroll
-      for (int c = 0; c < BC / 32; ++c) tmem_ld_32x32b_x32(tl + b * BC + c * 32, &sr[c * 32]);
+      for (int c = 0; c < BC / 32; ++c) tmem_ld_32x32b_x32(tS + c * 32, &sr[c * 32]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.s_free(b));
 
       float s[BC];
 #pragma unroll
       for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
       const int kv0 = (j_lo + it) * BC;
-      const bool edge = (kv0 + BC > N) || (r >= 0 && !(kv0 >= i0 + BR - 1 - r && kv0 + BC - 1 <= i0 + r));
+      const bool edge = (kv0 + BC > N) || (r >= 0 && !(kv0 >= qhi - r && kv0 + BC - 1 <= qlo + r));
       if (edge) {
 #pragma unroll
         for (int c = 0; c < BC; ++c) {
@@ -281,69 +308,83 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!valid) s[c] = -INFINITY;
         }
       }
-      float mx = s[0];
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
-      for (int c = 1; c < BC; ++c) mx = fmaxf(mx, s[c]);
-      const float mt = mx * sl;
+      for (int c = 4; c < BC; c += 4) {
+        mx0 = fmaxf(mx0, fmaxf(s[c], s[c + 1]));
+        mx1 = fmaxf(mx1, fmaxf(s[c + 2], s[c + 3]));
+      }
+      const float mt = fmaxf(mx0, mx1) * sl;
       float alpha = 1.f;
       if (mt > m_ref + kRescaleThreshold) {
         alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
         m_ref = mt;
       }
-      const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f;
-      uint32_t pk[BC / 2];
+      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      float rs0 = 0.f, rs1 = 0.f;
+      // P (bf16 pairs) over the first half of this tile's S columns, written in
+      // four groups of 16 columns as soon as each group is ready; S columns
+      // 32g..32g+31 were read above, before group g overwrites columns 16g..16g+15
 #pragma unroll
-      for (int c = 0; c < BC / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], sl, -mref));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl, -mref));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+      for (int g = 0; g < 4; ++g) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int e = 32 * g + 2 * c;
+          const float x0 = fmaf(s[e], sl, nref), x1 = fmaf(s[e + 1], sl, nref);
+          float p0, p1;
+          // one pair in four on the FMA pipe, the rest on the special-function
+          // unit; tiles with masked scores use the special-function unit only
+          if (!edge && (c & 3) == 3) {
+            p0 = exp2_poly(x0);
+            p1 = exp2_poly(x1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          rs0 += p0;
+          rs1 += p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_32x32b_x16(tS + 16 * g, pk);
       }
-      l = l * alpha + rs;
-
-      // P buffer and O accumulator are free once the previous P V has completed
-      if (it > 0) {
-        if (!warp_wait(bar.pv_done, (it - 1) & 1)) {
+      // O may be rescaled only once the previous P V into it has completed
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!warp_wait(bar.o_done(t), (it - 1) & 1)) {
+          tmem_wait_st();
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tl + kTmemO + c * 32, o);
-            tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_32x32b_x32(tl + kTmemO + c * 32, o);
-          }
-          tmem_wait_st();
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_32x32b_x32(tO + c * 32, o);
         }
       }
-      // P row -> shared memory, K-major 128-byte swizzled (same layout TMA gives Q)
-#pragma unroll
-      for (int c16 = 0; c16 < BC / 8; ++c16) {
-        const uint32_t addr = sP + (c16 >> 3) * (BR * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
-        st_shared_v4(addr, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full);
+      if (lane == 0) mbar_arrive(bar.p_full(t));
+      l = l * alpha + (rs0 + rs1);
     }
 
     // ------------------------------------------------------------ epilogue
-    const bool have = ok && warp_wait(bar.pv_done, (ntiles - 1) & 1);
+    const bool have = ok && warp_wait(bar.o_done(t), (ntiles - 1) & 1);
+    // the tile's Q buffer is idle once its last P V has completed: stage the
+    // bf16 O tile there, swizzled like the TMA layout of Q
+    const uint32_t sO = sQ + t * C::Q_BYTES;
     if (have) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      // stage the bf16 O tile in the (now idle) P buffer, swizzled like P
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tl + kTmemO + c * 32, o);
+        tmem_ld_32x32b_x32(tO + c * 32, o);
         tmem_wait_ld();
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -353,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
                                __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-          const uint32_t addr = sP + (c16 >> 3) * (BR * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+          const uint32_t addr = sO + (c16 >> 3) * (BR * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
           st_shared_v4(addr, w[0], w[1], w[2], w[3]);
         }
       }
@@ -363,15 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc_fence_before();
-    named_bar_sync(1, 128);  // reached by all four softmax warps on every path
+    named_bar_sync(1 + t, 128);  // reached by all four warps of the tile on every path
     if (have && !*abort_flag) {
       // coalesced 128-bit stores: consecutive threads write consecutive 16-byte chunks
       constexpr int CHUNKS = D / 8;
-      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * N + i0) * D * 2;
+      const int row0 = i0 + t * BR;
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * N + row0) * D * 2;
       for (int idx = row; idx < BR * CHUNKS; idx += 128) {
         const int rr = idx / CHUNKS, c16 = idx % CHUNKS;
-        if (i0 + rr < N) {
-          const uint4 val = ld_shared_v4(sP + (c16 >> 3) * (BR * 128) + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4));
+        if (row0 + rr < N) {
+          const uint4 val = ld_shared_v4(sO + (c16 >> 3) * (BR * 128) + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4));
           st_global_v4(obase + static_cast<size_t>(rr) * D * 2 + c16 * 16, val);
         }
       }
@@ -380,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -396,7 +438,7 @@ cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const long long nqt = (p.N + BR - 1) / BR;
+  const long long nqt = (p.N + 2 * BR - 1) / (2 * BR);
   const long long grid = nqt * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fa_fwd_bf16_sm103_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
