@@ -329,6 +329,7 @@ def main():
             "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
                        "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
                        "l2": "inputs larger than L2 (Q,K,V,O 4 x {:.0f} MB > 129 MB); no flush".format(
                            qd.numel() * 2 / 1e6)},
             "kernels": {n: {kk: round(vv, 4) for kk, vv in d.items()} for n, d in kernels.items()},

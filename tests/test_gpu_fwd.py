@@ -149,7 +149,8 @@ def test_full_size_workloads_sampled(index):
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
     vmax = vd.float().amax(dim=2, keepdim=True)
     vmin = vd.float().amin(dim=2, keepdim=True)
-    assert bool(((o.float() <= vmax + 1e-2) & (o.float() >= vmin - 1e-2)).all())
+    # convex hull of the value rows, up to the bf16 max-abs bar (the output is rounded to bf16)
+    assert bool(((o.float() <= vmax + 2e-2) & (o.float() >= vmin - 2e-2)).all())
     rng = np.random.default_rng(index)
     heads = [(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))]
     for b, h in heads:
