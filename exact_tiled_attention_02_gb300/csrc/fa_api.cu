@@ -250,6 +250,7 @@ fa_status fa_last_device_status(void* stream) {
   if (cudaMemsetAsync(sp, 0, sizeof(unsigned int), s) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
   if (host & sm103::kStatusTimeout) return FA_ERR_TIMEOUT;
+  if (host & sm103::kStatusLayout) return FA_ERR_CUDA;
   return FA_OK;
 }
 

@@ -38,7 +38,7 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;  // [B,H,N,d] fp32 workspace
-  float* lse2;    // [B,H,Npad] fp32 workspace: lse_i * log2(e) (+inf in padding rows)
+  float* lse2;    // [B,H,Npad] fp32 workspace: lse_i * log2(e) (+inf in padding rows), Npad = N rounded up to 128
   float* dsum;    // [B,H,Npad] fp32 workspace: D_i = sum_k dO_ik O_ik (0 in padding rows)
   int BH;
   int N;
@@ -64,14 +64,14 @@ cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
 // Byte size of the backward workspace and the offsets of its lse2 / dsum
-// sections (dq_acc is at offset 0); rows are padded to multiples of 64.
+// sections (dq_acc is at offset 0); rows are padded to multiples of 128.
 size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum);
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, cudaStream_t s);
 
 // Row counts of the tiles the TMA boxes use (host needs them for the maps).
 constexpr int kFwdBlockRows = 128;  // query rows per CTA tile
 constexpr int kFwdBlockCols = 128;  // keys per K/V tile
-constexpr int kBwdBlockRows = 64;   // query rows per step of the backward
+constexpr int kBwdBlockRows = 128;  // query rows per step of the backward
 constexpr int kBwdBlockCols = 128;  // keys per CTA of the backward
 
 }  // namespace fa

@@ -97,6 +97,7 @@ struct WaitCtl {
 };
 
 constexpr unsigned int kStatusTimeout = 4u;  // matches FA_ERR_TIMEOUT
+constexpr unsigned int kStatusLayout = 8u;   // a kernel refused to run: shared memory layout would not fit
 
 __device__ __forceinline__ void record_timeout(const WaitCtl& w) {
   if (w.abort_flag) *w.abort_flag = 1;

@@ -83,7 +83,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * Size in bytes of the workspace fa_bwd needs for a problem of this shape:
  * a float32 [B,H,N,d] dQ accumulator, then two float32 [B,H,Npad] arrays
  * (lse_i * log2(e) and D_i = sum_k dO_ik O_ik; Npad = N rounded up to a
- * multiple of 64), each section 256-byte aligned.  Returns 0 for
+ * multiple of 128), each section 256-byte aligned.  Returns 0 for
  * non-positive sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
@@ -112,7 +112,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 /*
  * Synchronises `stream` (as void* cudaStream_t), then reads and clears the
  * device status word that the kernels set when a bounded wait runs out.
- * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if synchronising failed.
+ * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if synchronising failed or a
+ * kernel refused to run on the device (a layout check failed).
  */
 fa_status fa_last_device_status(void* stream);
 

@@ -47,9 +47,9 @@ def test_workspace_size(b):
     n = b.fa_bwd_workspace_bytes(4, 16, 4096, 128)
     rows = 4 * 16 * 4096
     assert n >= rows * 128 * 4 + rows * 4 and n % 256 == 0
-    # dQ accumulator (15 floats -> 256 B), lse2 and D (64 padded rows each -> 256 B)
-    assert b.fa_bwd_workspace_bytes(1, 1, 3, 5) == 256 * 3
-    assert b.fa_bwd_workspace_bytes(2, 1, 65, 128) == 2 * 65 * 128 * 4 + 2 * (2 * 128 * 4)
+    # dQ accumulator (15 floats -> 256 B), lse2 and D (128 padded rows each -> 512 B)
+    assert b.fa_bwd_workspace_bytes(1, 1, 3, 5) == 256 + 512 + 512
+    assert b.fa_bwd_workspace_bytes(2, 1, 129, 128) == 2 * 129 * 128 * 4 + 2 * (2 * 256 * 4)
 
 
 def test_wait_limit_roundtrip(b):
