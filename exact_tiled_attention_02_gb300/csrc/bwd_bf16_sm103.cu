@@ -10,7 +10,7 @@
 // D_i = sum_j P_ij dP_ij = sum_k dO_ik O_ik, dQ = scale dS K, dK = scale dS^T Q.
 //
 // Three kernels:
-//   bwd_prep     D_i = rowsum(dO o O) and lse_i * log2(e) into the workspace
+//   bwd_prep     -D_i = -rowsum(dO o O) and -lse_i * log2(e) into the workspace
 //                (rows padded to a multiple of 128: D = 0, lse = +inf, so padded
 //                query rows get P = 0), and the fp32 dQ accumulator zeroed.
 //   bwd_main     one CTA per 128-key tile of one (batch, head): K_j, V_j stay
@@ -24,8 +24,11 @@
 //                  dQ^T = K_j^T dS^T       (shared memory, K_j^T and dS^T
 //                                           read MN-major)
 //                dV and dK accumulate in tensor memory for the whole loop; each
-//                dQ^T tile is added to the fp32 accumulator with coalesced
-//                atomic adds (32 consecutive d of one query row per warp op).
+//                dQ^T tile is staged as fp32 [128 queries][128 d] in the
+//                shared-memory stage its Q / dO tiles just vacated, and added to
+//                the fp32 accumulator by one TMA reduction (cp.reduce.async.bulk
+//                .tensor .add.f32), so the memory system does the adds in whole
+//                lines.
 //   bwd_dq       dQ = bf16(scale * accumulator).
 // (Measured on GB300: tcgen05.mma with M = 128 and K = 16 takes 64 cycles at
 // N = 128 but 48 at N = 64, so 64-row query tiles would waste a third of the
@@ -38,7 +41,10 @@
 //               (thread t owns key row t == TMEM lane t; for the dQ^T
 //               read-out it owns head-dimension index t)
 //   warp  8     TMEM owner + MMA issuer (one elected lane)
-//   warp  9     TMA / bulk-copy producer (one elected lane)
+//   warp  9     TMA producer (one elected lane): loads Q_i, dO_i, lse_i, D_i into
+//               a two-stage ring, issues the dQ^T reduction of tile i from
+//               stage i%2 and refills that stage with tile i+2 once the
+//               reduction has read it
 //   warps 10-11 idle
 // Tensor memory columns (128 lanes each):
 //   [0,128)   S^T; warpgroup g writes its bf16 P^T over [64g, 64g+32);
@@ -75,8 +81,8 @@ constexpr int STAGE_BYTES = 2 * TILE_BYTES;
 constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr int OFF_VEC = OFF_DST + TILE_BYTES;
 constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
-// kv_full, q_full[2], q_empty[2], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain
-constexpr int NBAR = 1 + 2 * STAGES + 8;
+// kv_full, q_full[2], staged[2], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done
+constexpr int NBAR = 1 + 2 * STAGES + 9;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = 227 * 1024;  // the whole opt-in budget; the kernel checks the alignment pad fits
@@ -87,7 +93,7 @@ struct Bars {
   uint32_t base;
   __device__ uint32_t kv_full() const { return base; }
   __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t q_empty(int s) const { return base + 8 * (1 + STAGES + s); }
+  __device__ uint32_t staged(int s) const { return base + 8 * (1 + STAGES + s); }
   __device__ uint32_t s_full() const { return base + 8 * (1 + 2 * STAGES); }
   __device__ uint32_t dp_full() const { return base + 8 * (2 + 2 * STAGES); }
   __device__ uint32_t p_full() const { return base + 8 * (3 + 2 * STAGES); }
@@ -96,6 +102,7 @@ struct Bars {
   __device__ uint32_t dq_free() const { return base + 8 * (6 + 2 * STAGES); }
   __device__ uint32_t fin() const { return base + 8 * (7 + 2 * STAGES); }
   __device__ uint32_t drain() const { return base + 8 * (8 + 2 * STAGES); }
+  __device__ uint32_t prod_done() const { return base + 8 * (9 + 2 * STAGES); }
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   const int i = static_cast<int>(row % np);
   if (i >= N) {
     if (lane == 0) {
-      lse2[row] = INFINITY;
+      lse2[row] = -INFINITY;
       dsum[row] = 0.f;
     }
     return;
@@ -140,8 +147,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
-    dsum[row] = acc;
-    lse2[row] = lse[bh * N + i] * 1.4426950408889634f;
+    dsum[row] = -acc;
+    lse2[row] = -lse[bh * N + i] * 1.4426950408889634f;
   }
   float4* z = reinterpret_cast<float4*>(dq_acc + src);
   for (int c = lane; c < d / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -170,7 +177,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                             const BwdParams p) {
+                             const __grid_constant__ CUtensorMap tmdq, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.kv_full(), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar.q_full(s), 1);
-      mbar_init(bar.q_empty(s), 1);
+      mbar_init(bar.staged(s), 8);  // one arrive per compute warp
     }
     mbar_init(bar.s_full(), 1);
     mbar_init(bar.dp_full(), 1);
@@ -216,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.dq_free(), 8);
     mbar_init(bar.fin(), 1);
     mbar_init(bar.drain(), 1);
+    mbar_init(bar.prod_done(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -242,15 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
       prefetch_tensormap(&tmdo);
+      prefetch_tensormap(&tmdq);
       mbar_arrive_expect_tx(bar.kv_full(), 2 * TILE_BYTES);
       for (int b = 0; b < 2; ++b) {
         tma_load_3d(sK + b * BOX_BYTES, &tmk, bar.kv_full(), b * 64, k0, bh);
         tma_load_3d(sV + b * BOX_BYTES, &tmv, bar.kv_full(), b * 64, k0, bh);
       }
-      int issued = 0;
-      for (int it = 0; it < nsteps; ++it) {
+      auto load = [&](int it) {
         const int st = it % STAGES;
-        if (!mbar_wait(bar.q_empty(st), ((it / STAGES) & 1) ^ 1, wc)) break;
         const int q0 = (t_lo + it) * BM;
         const uint32_t base = sStage + st * STAGE_BYTES;
         const uint32_t vec = sVec + st * 2 * VEC_BYTES;
@@ -262,14 +269,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t vrow = static_cast<size_t>(bh) * np + q0;
         bulk_load(vec, p.lse2 + vrow, VEC_BYTES, bar.q_full(st));
         bulk_load(vec + VEC_BYTES, p.dsum + vrow, VEC_BYTES, bar.q_full(st));
-        issued = it + 1;
+      };
+      int loaded = 0;
+      for (; loaded < STAGES && loaded < nsteps; ++loaded) load(loaded);
+      for (int it = 0; it < nsteps; ++it) {
+        // tile it's dQ^T is staged in stage it%2: reduce it into the accumulator,
+        // then reuse the stage for tile it+2 once the reduction has read it
+        const int st = it % STAGES;
+        if (!mbar_wait(bar.staged(st), (it / STAGES) & 1, wc)) break;
+        tma_reduce_add_3d(&tmdq, sStage + st * STAGE_BYTES, 0, (t_lo + it) * BM, bh);
+        bulk_commit_group();
+        if (loaded < nsteps) {
+          bulk_wait_read_all();
+          load(loaded);
+          ++loaded;
+        }
       }
+      bulk_wait_all();  // reductions complete (and their sources read) before the stages are reused or the CTA exits
       if (*abort_flag) {
         WaitCtl drain{nullptr, nullptr, wc.limit_ns};
         mbar_wait(bar.kv_full(), 0, drain);
-        for (int it = max(0, issued - STAGES); it < issued; ++it)
+        for (int it = max(0, loaded - STAGES); it < loaded; ++it)
           mbar_wait(bar.q_full(it % STAGES), (it / STAGES) & 1, drain);
       }
+      mbar_arrive(bar.prod_done());
     }
     __syncwarp();
   } else if (warp == 8) {
@@ -322,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + TM_S, sdesc_sw128(sK + kk * 2048, BOX_BYTES, 1024),
                       sdesc_sw128(sDS + kk * 2048, BOX_BYTES, 1024), id_mm, kk > 0);
         mma_commit(bar.dq_full());
-        mma_commit(bar.q_empty(st));
         // next tile's S^T and dP^T once dQ^T has been read out of the S^T columns
         if (i + 1 < nsteps) {
           if (!mbar_wait(bar.dq_free(), ph, wc)) break;
@@ -345,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t tS = tl + TM_S + 64 * g, tDP = tl + TM_DP + 64 * g;
     const uint32_t sDSg = sDS + g * BOX_BYTES;
-    const float sl = p.scale_log2;
-    const bool key_ok = kj < N;
-    float* acc_base = p.dq_acc + static_cast<size_t>(bh) * N * D + row;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    // Key rows past N hold zeros (TMA zero fill): their P and dS are finite and
+    // meet K = 0 in dQ; their dK / dV rows are never stored.  No mask needed.
     bool ok = true;
     for (int i = 0; i < nsteps; ++i) {
       const uint32_t ph = i & 1;
@@ -363,21 +385,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_32x32b_x32(tS, &sv[0]);
       tmem_ld_32x32b_x32(tS + 32, &sv[32]);
       tmem_wait_ld();
-      const float4* lse4 = reinterpret_cast<const float4*>(smem + OFF_VEC + st * 2 * VEC_BYTES + 64 * 4 * g);
-      const float4* dsv4 = reinterpret_cast<const float4*>(smem + OFF_VEC + st * 2 * VEC_BYTES + VEC_BYTES + 64 * 4 * g);
-      const bool edge = r >= 0 && !(q0 >= kj - r && q0 + 63 <= kj + r);
+      const float4* nlse4 = reinterpret_cast<const float4*>(smem + OFF_VEC + st * 2 * VEC_BYTES + 64 * 4 * g);
+      const float4* nd4 = reinterpret_cast<const float4*>(smem + OFF_VEC + st * 2 * VEC_BYTES + VEC_BYTES + 64 * 4 * g);
       float pr[64];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = lse4[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float4 l4 = nlse4[c4];
+        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), sl2,
+                                     make_float2(l4.x, l4.y));
+        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])), sl2,
+                                     make_float2(l4.z, l4.w));
+        pr[4 * c4] = ex2_approx(x0.x);
+        pr[4 * c4 + 1] = ex2_approx(x0.y);
+        pr[4 * c4 + 2] = ex2_approx(x1.x);
+        pr[4 * c4 + 3] = ex2_approx(x1.y);
+      }
+      if (r >= 0 && !(q0 >= kj - r && q0 + 63 <= kj + r)) {  // window: zero the out-of-band pairs
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          float pv = ex2_approx(fmaf(__uint_as_float(sv[c]), sl, -lv[e]));
-          if (edge && abs(q0 + c - kj) > r) pv = 0.f;
-          pr[c] = key_ok ? pv : 0.f;
-        }
+        for (int c = 0; c < 64; ++c)
+          if (abs(q0 + c - kj) > r) pr[c] = 0.f;
       }
       {
         uint32_t pk[32];
@@ -403,18 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t dk[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const float4 da = dsv4[2 * c8], db = dsv4[2 * c8 + 1];
-          const float dv8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 n4 = nd4[c4];
+          const float2 t0 = __fadd2_rn(make_float2(__uint_as_float(dpv[4 * c4]), __uint_as_float(dpv[4 * c4 + 1])),
+                                       make_float2(n4.x, n4.y));
+          const float2 t1 = __fadd2_rn(make_float2(__uint_as_float(dpv[4 * c4 + 2]), __uint_as_float(dpv[4 * c4 + 3])),
+                                       make_float2(n4.z, n4.w));
+          const float2 d0 = __fmul2_rn(make_float2(pr[4 * c4], pr[4 * c4 + 1]), t0);
+          const float2 d1 = __fmul2_rn(make_float2(pr[4 * c4 + 2], pr[4 * c4 + 3]), t1);
+          dk[2 * c4] = pack_bf16x2(d0.x, d0.y);
+          dk[2 * c4 + 1] = pack_bf16x2(d1.x, d1.y);
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * c8 + 2 * e;
-            dk[4 * c8 + e] = pack_bf16x2(pr[c] * (__uint_as_float(dpv[c]) - dv8[2 * e]),
-                                         pr[c + 1] * (__uint_as_float(dpv[c + 1]) - dv8[2 * e + 1]));
-          }
+        for (int c8 = 0; c8 < 8; ++c8)
           st_shared_v4(sDSg + row * 128 + ((c8 ^ (row & 7)) << 4), dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2],
                        dk[4 * c8 + 3]);
-        }
         tmem_st_32x32b_x32(tDP, dk);  // dS^T over this warpgroup's first 32 dP^T columns
       }
       fence_proxy_async_smem();
@@ -423,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_full());
 
-      // ---- dQ^T read-out (thread = head-dimension index) and fp32 reduction
+      // ---- dQ^T read-out (thread = head-dimension index), staged as fp32
+      //      [query][d] in stage i%2 (its Q_i / dO_i were last read by dK_i and
+      //      dV_i, both complete once dQ^T is), for the producer's TMA reduction
       if (!warp_wait(bar.dq_full(), ph)) {
         ok = false;
         break;
@@ -436,16 +467,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.dq_free());
-      const int cnt = min(64, N - q0);
+      float* stg = reinterpret_cast<float*>(smem + OFF_STAGE + st * STAGE_BYTES) + (64 * g) * D + row;
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c < cnt) red_add_f32(acc_base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+      for (int c = 0; c < 64; ++c) stg[c * D] = __uint_as_float(qv[c]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.staged(st));
     }
 
     // ------------------------------------------------------------ epilogue
     // warpgroup 0 writes dV, warpgroup 1 writes scale * dK, each staged as a
     // bf16 [128 keys][128 d] tile in an idle Q/dO stage
-    const bool have = ok && warp_wait(bar.fin(), 0);
+    const bool have = ok && warp_wait(bar.fin(), 0) && warp_wait(bar.prod_done(), 0);
     const uint32_t stage_out = sStage + g * STAGE_BYTES;
     if (have) {
       tc_fence_after();
@@ -523,7 +556,7 @@ cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_
       p.dq_acc, p.BH, p.N, p.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_bf16_sm103_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, p);
+  fa_bwd_bf16_sm103_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, m.dq_acc, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(

@@ -83,6 +83,20 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int BH, int N, int d, int b
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 [BH, N, d] dQ accumulator for TMA reductions: dims
+// (d, N, BH), box (d, rows, 1), no swizzle; rows past N are not written.
+bool make_map_f32_acc(CUtensorMap* m, const void* base, int BH, int N, int d, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Host-side validation shared by forward and backward; runs before any CUDA
@@ -234,7 +248,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
   BwdMaps m;
   if (!make_map_bf16(&m.q, q, p.BH, N, d, kBwdBlockRows) || !make_map_bf16(&m.k, k, p.BH, N, d, kBwdBlockCols) ||
-      !make_map_bf16(&m.v, v, p.BH, N, d, kBwdBlockCols) || !make_map_bf16(&m.dO, dO, p.BH, N, d, kBwdBlockRows))
+      !make_map_bf16(&m.v, v, p.BH, N, d, kBwdBlockCols) || !make_map_bf16(&m.dO, dO, p.BH, N, d, kBwdBlockRows) ||
+      !make_map_f32_acc(&m.dq_acc, p.dq_acc, p.BH, N, d, kBwdBlockRows))
     return FA_ERR_CUDA;
   const cudaError_t e = launch_bwd_bf16_tc(p, m, s);
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;

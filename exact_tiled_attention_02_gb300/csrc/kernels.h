@@ -38,8 +38,8 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;  // [B,H,N,d] fp32 workspace
-  float* lse2;    // [B,H,Npad] fp32 workspace: lse_i * log2(e) (+inf in padding rows), Npad = N rounded up to 128
-  float* dsum;    // [B,H,Npad] fp32 workspace: D_i = sum_k dO_ik O_ik (0 in padding rows)
+  float* lse2;    // [B,H,Npad] fp32 workspace: -lse_i * log2(e) (-inf in padding rows), Npad = N rounded up to 128
+  float* dsum;    // [B,H,Npad] fp32 workspace: -D_i = -sum_k dO_ik O_ik (0 in padding rows)
   int BH;
   int N;
   int d;
@@ -57,6 +57,7 @@ struct FwdMaps {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO;
+  CUtensorMap dq_acc;  // fp32 [BH, N, d] accumulator: dims (d, N, BH), box (d, 128, 1), no swizzle
 };
 
 // Launchers (each returns the launch's cudaError_t).
