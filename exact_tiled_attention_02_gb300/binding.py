@@ -19,8 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libfa.so")
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_device_status", "fa_set_wait_limit_us",
-           "fa_selftest_wait_timeout", "fa_status_string", "fa_version")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_static_workspace", "fa_last_device_status",
+           "fa_set_wait_limit_us", "fa_selftest_wait_timeout", "fa_status_string", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -39,6 +39,8 @@ def _load() -> ctypes.CDLL:
     L.fa_fwd.restype = i
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd.restype = i
+    L.fa_bwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_static_workspace.restype = i
     L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_bwd_workspace_bytes.restype = sz
     L.fa_last_device_status.argtypes = [vp]
@@ -177,4 +179,24 @@ def fa_bwd(q, k, v, o, lse, do, scale: float | None = None, window: int = 0, dq=
                     workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_static_workspace(q, k, v, o, lse, do, dq, dk, dv, scale: float | None = None, window: int = 0,
+                            stream=None):
+    """fa_bwd without a workspace argument, for callers that cannot allocate
+    device memory: the library's fixed 64 MiB scratch array stands in for the
+    workspace, and neither this wrapper nor the library allocates anything
+    (the caller passes the dq, dk, dv outputs).  Calls that overlap on the GPU
+    share that array and race; problems needing more than 64 MiB of workspace
+    raise FaError(FA_ERR_UNSUPPORTED)."""
+    _check_qkv(q, k, v, o, do, dq, dk, dv)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib.fa_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), B, H, N, d, float(scale), int(window), _dtype_code(q),
+                                     _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_static_workspace")
     return dq, dk, dv

@@ -110,6 +110,26 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd for callers that cannot allocate device memory (code running where
+ * device allocation is not permitted, or with no allocator to call): the same
+ * arguments and results as fa_bwd, minus the workspace, which is replaced by
+ * a fixed 64 MiB scratch array inside the library (reserved on every GPU that
+ * loads the library, until the process exits).  This function allocates
+ * nothing.  The pages describe no such variant; it is a deployment aid.
+ *   - Problems with fa_bwd_workspace_bytes(B,H,N,d) > 64 MiB return
+ *     FA_ERR_UNSUPPORTED before anything is launched.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (e.g. on two concurrent streams) race on it; calls in order on one
+ *     stream are fine.  Each call re-initialises what must start at zero.
+ *   - The first call on each device looks up the array's device address;
+ *     make that first call before any stream capture.
+ */
+fa_status fa_bwd_static_workspace(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                  int B, int H, int N, int d, float scale, int window, fa_dtype dt,
+                                  void* stream);
+
+/*
  * Synchronises `stream` (as void* cudaStream_t), then reads and clears the
  * device status word that the kernels set when a bounded wait runs out.
  * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if synchronising failed or a
