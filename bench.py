@@ -192,6 +192,17 @@ def oracle_sample(w, q, k, v, do, with_bwd, budget_s: float, max_heads=None, row
     return done_f, t_total, heads
 
 
+def data_desc(w):
+    return "synthetic (seeded standard normals" + (f", Q,K x{w.qk_mult:g}" if w.qk_mult != 1.0 else "") + ")"
+
+
+def l2_note(w, qd):
+    total = 4 * qd.numel() * qd.element_size()
+    if total > L2_BYTES:
+        return f"inputs larger than L2 (Q,K,V,O {total / 1e6:.0f} MB > 129 MB); no flush"
+    return f"inputs smaller than L2 ({total / 1e6:.2f} MB); no flush (latency-bound case)"
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -325,13 +336,12 @@ def main():
             "metric": "attention TFLOP/s (fwd 4*B*H*N^2*d" + (" + bwd 2.5x" if with_bwd else "") + ")",
             "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded standard normals, Q,K x8)",
+            "vs_baseline": None, "dtype": w.dtype, "data": data_desc(w),
             "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
                        "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
-                       "l2": "inputs larger than L2 (Q,K,V,O 4 x {:.0f} MB > 129 MB); no flush".format(
-                           qd.numel() * 2 / 1e6)},
+                       "l2": l2_note(w, qd)},
             "kernels": {n: {kk: round(vv, 4) for kk, vv in d.items()} for n, d in kernels.items()},
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -426,7 +436,7 @@ def run_reference(args, w, world):
         "metric": "attention TFLOP/s (fwd 4*B*H*N^2*d" + (" + bwd 2.5x" if with_bwd else "") + ")",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic (seeded standard normals, Q,K x8)", "impl": "reference",
+        "dtype": "f64", "data": data_desc(w), "impl": "reference",
         "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
                    "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
