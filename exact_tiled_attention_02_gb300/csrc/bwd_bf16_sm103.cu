@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile it's dQ^T is staged in stage it%2: reduce it into the accumulator,
         // then reuse the stage for tile it+2 once the reduction has read it
         const int st = it % STAGES;
-        if (!mbar_wait(bar.staged(st), (it / STAGES) & 1, wc)) break;
+        if (!mbar_wait_backoff(bar.staged(st), (it / STAGES) & 1, wc)) break;
         tma_reduce_add_3d(&tmdq, sStage + st * STAGE_BYTES, 0, (t_lo + it) * BM, bh);
         bulk_commit_group();
         if (loaded < nsteps) {

@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < ntiles; ++it) {
         const int st = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1;
-        if (!mbar_wait(bar.kv_empty(st), ph ^ 1, wc)) break;
+        if (!mbar_wait_backoff(bar.kv_empty(st), ph ^ 1, wc)) break;
         const int kv0 = (j_lo + it) * BC;
         mbar_arrive_expect_tx(bar.k_full(st), C::KV_BYTES);
 #pragma unroll
@@ -334,15 +334,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        // one TMEM round trip: all D columns loaded, scaled, stored back
+        uint32_t o[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + c * 32, o);
-          tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) tmem_ld_32x32b_x32(tO + c * 32, &o[c * 32]);
+        tmem_wait_ld();
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_32x32b_x32(tO + c * 32, o);
+        for (int e = 0; e < D; e += 2) {
+          const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+          o[e] = __float_as_uint(v.x);
+          o[e + 1] = __float_as_uint(v.y);
         }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_st_32x32b_x32(tO + c * 32, &o[c * 32]);
       }
       tmem_wait_st();
       tc_fence_before();

@@ -152,6 +152,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// mbar_wait for a thread whose latency matters little (the TMA producer):
+// between polls it sleeps, so it does not take issue slots from the compute
+// warps that share its SM sub-partition.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(128);
+      if (mbar_try_wait(bar, parity)) return true;
+    }
+    if (w.abort_flag && *w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      record_timeout(w);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (no multicast): 3-D tiled tensor load into shared memory, completion
 // counted in bytes on an mbarrier.
