@@ -400,10 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         pr[4 * c4 + 2] = ex2_approx(x1.x);
         pr[4 * c4 + 3] = ex2_approx(x1.y);
       }
-      if (r >= 0 && !(q0 >= kj - r && q0 + 63 <= kj + r)) {  // window: zero the out-of-band pairs
+      if (r >= 0 && !(q0 >= kj - r && q0 + 63 <= kj + r)) {
+        // window: the queries that see key kj form one contiguous column range [lo, hi)
+        const int lo = max(0, kj - r - q0), hi = min(64, kj + r + 1 - q0);
+        const unsigned span = hi > lo ? static_cast<unsigned>(hi - lo) : 0u;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (abs(q0 + c - kj) > r) pr[c] = 0.f;
+        for (int c = 0; c < 64; ++c) pr[c] = (static_cast<unsigned>(c - lo) < span) ? pr[c] : 0.f;
       }
       {
         uint32_t pk[32];

@@ -90,7 +90,9 @@ struct Bars {
   __device__ uint32_t drain() const { return base + 8 * (8 + 3 * STAGES); }
 };
 
-template <int D>
+// WIN: compiled for a local window (band masks, per-tile key ranges); the
+// unmasked instantiation carries none of that code.
+template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
@@ -107,20 +109,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = p.N;
-  const int r = p.window_r;
+  const int r = WIN ? p.window_r : -1;
   const int nqt = (N + 2 * BR - 1) / (2 * BR);
   const int bh = blockIdx.x / nqt;
   const int i0 = (blockIdx.x % nqt) * (2 * BR);  // first row of Q0; Q1 starts at i0 + BR
 
   // key tiles the two query tiles need (only in-band tiles when windowed)
   int j_lo = 0, j_hi = (N + BC - 1) / BC;
-  if (r >= 0) {
+  if (WIN) {
     const int lo = max(0, i0 - r);
     const int hi = min(N, i0 + 2 * BR + r);  // exclusive
     j_lo = lo / BC;
     j_hi = (hi + BC - 1) / BC;
   }
   const int ntiles = j_hi - j_lo;
+  // each query tile's own key-tile range, as offsets into [j_lo, j_hi): with a
+  // window, a tile skips the union's tiles that lie wholly outside its band
+  auto tile_range = [&](int t, int& lo, int& hi) {
+    lo = 0;
+    hi = ntiles;
+    const int row_lo = i0 + t * BR, row_hi = min(N, row_lo + BR) - 1;
+    if (WIN) {
+      if (row_lo >= N) {
+        hi = 0;  // no rows: nothing to compute or store
+      } else {
+        lo = max(0, row_lo - r) / BC - j_lo;
+        hi = (min(N, row_hi + r + 1) + BC - 1) / BC - j_lo;
+      }
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -209,42 +226,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar.s_full(t));
       };
-      auto issue_pv = [&](int t, int it) {  // O_t += P_t V_it
+      auto issue_pv = [&](int t, int it, bool first) {  // O_t (+)= P_t V_it
         const uint32_t vbase = sV + (it % C::STAGES) * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
           mma_bf16_ts(tmem + kTmemO + t * 128, tmem + kTmemS + t * 128 + kk * 8,
-                      sdesc_sw128(vbase + kk * 16 * 128, BC * 128, 1024), idesc_pv, (it > 0 || kk > 0));
+                      sdesc_sw128(vbase + kk * 16 * 128, BC * 128, 1024), idesc_pv, (!first || kk > 0));
         mma_commit(bar.o_done(t));
       };
-      bool ok = mbar_wait(bar.q_full(0), 0, wc) && mbar_wait(bar.k_full(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        ok = mbar_wait(bar.q_full(1), 0, wc);
+      auto wait_k = [&](int it) { return mbar_wait(bar.k_full(it % C::STAGES), (it / C::STAGES) & 1, wc); };
+      if constexpr (!WIN) {
+        // both tiles take every key tile: PV0(j), S0(j+1), PV1(j), release, S1(j+1)
+        bool ok = mbar_wait(bar.q_full(0), 0, wc) && wait_k(0);
         if (ok) {
           tc_fence_after();
-          issue_s(1, 0);
+          issue_s(0, 0);
+          ok = mbar_wait(bar.q_full(1), 0, wc);
+          if (ok) {
+            tc_fence_after();
+            issue_s(1, 0);
+          }
         }
-      }
-      for (int it = 0; ok && it < ntiles; ++it) {
-        const int st = it % C::STAGES;
-        const uint32_t ph = (it / C::STAGES) & 1;
-        const bool more = it + 1 < ntiles;
-        if (!mbar_wait(bar.v_full(st), ph, wc)) break;
-        if (!mbar_wait(bar.p_full(0), it & 1, wc)) break;
-        tc_fence_after();
-        issue_pv(0, it);
-        if (more) {
-          if (!mbar_wait(bar.k_full((it + 1) % C::STAGES), ((it + 1) / C::STAGES) & 1, wc)) break;
+        for (int it = 0; ok && it < ntiles; ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          const bool more = it + 1 < ntiles;
+          if (!mbar_wait(bar.v_full(st), ph, wc)) break;
+          if (!mbar_wait(bar.p_full(0), it & 1, wc)) break;
           tc_fence_after();
-          issue_s(0, it + 1);
+          issue_pv(0, it, it == 0);
+          if (more) {
+            if (!wait_k(it + 1)) break;
+            tc_fence_after();
+            issue_s(0, it + 1);
+          }
+          if (!mbar_wait(bar.p_full(1), it & 1, wc)) break;
+          tc_fence_after();
+          issue_pv(1, it, it == 0);
+          mma_commit(bar.kv_empty(st));  // before S1(j+1): a commit waits for every earlier MMA
+          if (more) issue_s(1, it + 1);
         }
-        if (!mbar_wait(bar.p_full(1), it & 1, wc)) break;
-        tc_fence_after();
-        issue_pv(1, it);
-        mma_commit(bar.kv_empty(st));
-        if (more) issue_s(1, it + 1);
+      } else {
+        // windowed: each tile only over its own key range
+        int t_lo[2], t_hi[2];
+        tile_range(0, t_lo[0], t_hi[0]);
+        tile_range(1, t_lo[1], t_hi[1]);
+        bool ok = true;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || t_lo[t] >= t_hi[t]) continue;
+          ok = mbar_wait(bar.q_full(t), 0, wc) && wait_k(t_lo[t]);
+          if (ok) {
+            tc_fence_after();
+            issue_s(t, t_lo[t]);
+          }
+        }
+        int cnt[2] = {0, 0};
+        for (int it = 0; ok && it < ntiles; ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(bar.v_full(st), ph, wc)) break;
+          bool k_next = false;  // K tile it+1 known to be resident
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || it < t_lo[t] || it >= t_hi[t]) continue;
+            if (!mbar_wait(bar.p_full(t), cnt[t] & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, it, cnt[t] == 0);
+            ++cnt[t];
+            // release the K/V slot right after the last product that reads V_it
+            // (a commit waits for every earlier MMA, so it must precede S_t(it+1))
+            if (t == 1 || it < t_lo[1] || it >= t_hi[1]) mma_commit(bar.kv_empty(st));
+            if (it + 1 < t_hi[t]) {
+              if (!k_next && !(k_next = wait_k(it + 1))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(t, it + 1);
+            }
+          }
+        }
       }
       // every MMA this thread issued must finish before tensor memory is freed
       mma_commit(bar.drain());
@@ -268,8 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto warp_wait = [&](uint32_t bar_addr, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
     };
-    for (int it = 0; it < ntiles; ++it) {
-      if (!warp_wait(bar.s_full(t), it & 1)) {
+    int my_lo = 0, my_hi = ntiles;
+    if constexpr (WIN) tile_range(t, my_lo, my_hi);
+    for (int it = my_lo; it < my_hi; ++it) {
+      const int n = it - my_lo;  // tiles this warpgroup has processed
+      if (!warp_wait(bar.s_full(t), n & 1)) {
         ok = false;
         break;
       }
@@ -283,14 +351,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
       const int kv0 = (j_lo + it) * BC;
-      const bool edge = (kv0 + BC > N) || (r >= 0 && !(kv0 >= qhi - r && kv0 + BC - 1 <= qlo + r));
+      const bool edge = (kv0 + BC > N) || (WIN && !(kv0 >= qhi - r && kv0 + BC - 1 <= qlo + r));
       if (edge) {
-#pragma unroll
-        for (int c = 0; c < BC; ++c) {
-          const int kv = kv0 + c;
-          const bool valid = kv < N && (r < 0 || abs(qi - kv) <= r);
-          if (!valid) s[c] = -INFINITY;
+        // the visible keys of row qi form one contiguous column range [lo, hi)
+        int lo = 0, hi = min(BC, N - kv0);
+        if (WIN) {
+          lo = max(lo, qi - r - kv0);
+          hi = min(hi, qi + r + 1 - kv0);
         }
+        const unsigned span = hi > lo ? static_cast<unsigned>(hi - lo) : 0u;
+#pragma unroll
+        for (int c = 0; c < BC; ++c) s[c] = (static_cast<unsigned>(c - lo) < span) ? s[c] : -INFINITY;
       }
       // row maximum: four independent chains of three-input max
       float mx[4];
@@ -327,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y) + (rs[2].x + rs[2].y) + (rs[3].x + rs[3].y);
       // O may be rescaled only once the previous P V into it has completed
-      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!warp_wait(bar.o_done(t), (it - 1) & 1)) {
+      if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
           tmem_wait_st();
           ok = false;
           break;
@@ -357,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    const bool have = ok && warp_wait(bar.o_done(t), (ntiles - 1) & 1);
+    const bool have = ok && my_lo < my_hi && warp_wait(bar.o_done(t), (my_hi - my_lo - 1) & 1);
     // the tile's Q buffer is idle once its last P V has completed: stage the
     // bf16 O tile there, swizzled like the TMA layout of Q
     const uint32_t sO = sQ + t * C::Q_BYTES;
@@ -411,28 +482,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool WIN>
 cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
   using C = Cfg<D>;
   static bool configured = false;  // attribute set once per process (one device per process in practice)
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_sm103_kernel<D, WIN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const long long nqt = (p.N + 2 * BR - 1) / (2 * BR);
   const long long grid = nqt * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_bf16_sm103_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
+  fa_fwd_bf16_sm103_kernel<D, WIN><<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
-  if (p.d == 128) return launch_d<128>(p, m, s);
-  if (p.d == 64) return launch_d<64>(p, m, s);
+  const bool win = p.window_r >= 0;
+  if (p.d == 128) return win ? launch_d<128, true>(p, m, s) : launch_d<128, false>(p, m, s);
+  if (p.d == 64) return win ? launch_d<64, true>(p, m, s) : launch_d<64, false>(p, m, s);
   return cudaErrorInvalidValue;
 }
 
