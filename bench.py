@@ -203,6 +203,24 @@ def l2_note(w, qd):
     return f"inputs smaller than L2 ({total / 1e6:.2f} MB); no flush (latency-bound case)"
 
 
+def dist_max(x: float, pg=None, device=None) -> float:
+    """Maximum of ``x`` over all ranks (the slowest rank sets the step time);
+    ``x`` itself when there is no process group."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own full workload (heads
+    are independent problems), so the job does world x the work of one rank
+    in the slowest rank's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -294,17 +312,14 @@ def main():
     total_ms = start.elapsed_time(end)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if with_bwd else None
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = dist_max(total_ms, pg, dev)
     assert fa.fa_last_device_status() == fa.FA_OK, "a device-side wait timed out during the bench"
 
     ms_per_step = total_ms / K
     flops_fwd = w.fwd_flops()
     flops_bwd = w.bwd_flops() if with_bwd else 0.0
     flops_step = flops_fwd + flops_bwd
-    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+    value = weak_scaling_value(flops_step, world, ms_per_step)
 
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"]
@@ -397,17 +412,13 @@ def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = dist_max(a.elapsed_time(b) / steps, pg, dev)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     flops = w.fwd_flops() + (w.bwd_flops() if with_bwd else 0.0)
     elem = q.numel() * q.element_size()
     h2d = 3 * elem + (elem if with_bwd else 0)
     d2h = elem + w.B * w.H * w.N * 4 + (3 * elem if with_bwd else 0)
-    return {"value": round(flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+    return {"value": round(weak_scaling_value(flops, world, ms), 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
