@@ -21,14 +21,14 @@
 //                  dP^T = V_j dO_i^T       (shared memory)
 //                  dV  += P^T dO_i         (P^T from tensor memory)
 //                  dK  += dS^T Q_i         (dS^T from tensor memory)
-//                  dQ^T = K_j^T dS^T       (shared memory, K_j^T and dS^T
-//                                           read MN-major)
+//                  dQ   = dS K_j          (shared memory: dS^T and K_j read
+//                                           MN-major; TMEM lanes = queries)
 //                dV and dK accumulate in tensor memory for the whole loop; each
-//                dQ^T tile is staged as fp32 [128 queries][128 d] in the
-//                shared-memory stage its Q / dO tiles just vacated, and added to
-//                the fp32 accumulator by one TMA reduction (cp.reduce.async.bulk
-//                .tensor .add.f32), so the memory system does the adds in whole
-//                lines.
+//                dQ tile is staged as fp32 [128 queries][128 d] (four 128-byte-
+//                swizzled boxes of 32 columns) in the shared-memory stage its
+//                Q / dO tiles just vacated, and added to the fp32 accumulator
+//                by TMA reductions (cp.reduce.async.bulk.tensor .add.f32), so
+//                the memory system does the adds in whole lines.
 //   bwd_dq       dQ = bf16(scale * accumulator).
 // (Measured on GB300: tcgen05.mma with M = 128 and K = 16 takes 64 cycles at
 // N = 128 but 48 at N = 64, so 64-row query tiles would waste a third of the
@@ -38,8 +38,8 @@
 // group, so the two idle warps cost nothing):
 //   warps 0-3   compute warpgroup 0: query columns 0-63 of every tile
 //   warps 4-7   compute warpgroup 1: query columns 64-127
-//               (thread t owns key row t == TMEM lane t; for the dQ^T
-//               read-out it owns head-dimension index t)
+//               (thread t owns key row t == TMEM lane t; for the dQ
+//               read-out it owns query row t)
 //   warp  8     TMEM owner + MMA issuer (one elected lane)
 //   warp  9     TMA producer (one elected lane): loads Q_i, dO_i, lse_i, D_i into
 //               a two-stage ring, issues the dQ^T reduction of tile i from
@@ -48,7 +48,7 @@
 //   warps 10-11 idle
 // Tensor memory columns (128 lanes each):
 //   [0,128)   S^T; warpgroup g writes its bf16 P^T over [64g, 64g+32);
-//             then dQ^T of the same tile (written after dV has read P^T)
+//             then dQ of the same tile (written after dV has read P^T)
 //   [128,256) dP^T; warpgroup g writes its bf16 dS^T over [128+64g, 128+64g+32)
 //   [256,384) dV      [384,512) dK
 // tcgen05.mma operations issued by one thread execute in order, so a product
@@ -72,6 +72,7 @@ constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
 constexpr int TILE_BYTES = 128 * D * 2;   // 32 KB: a bf16 [128 x 128] tile as two 64-column boxes
 constexpr int BOX_BYTES = 128 * 128;      // 16 KB: one [128 rows x 64 cols] box
 constexpr int VEC_BYTES = BM * 4;         // 512 B of lse*log2e or of D
+constexpr int DQ_BOX_BYTES = BM * 32 * 4; // 16 KB: fp32 dQ staging box [128 queries][32 d], 128-byte swizzled
 // 1024-aligned region: K, V, stage 0 (Q, dO), stage 1 (Q, dO), dS^T; then the
 // small items (per-stage lse2 / D vectors, barriers, tmem slot, abort flag)
 constexpr int OFF_K = 0;
@@ -277,7 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // then reuse the stage for tile it+2 once the reduction has read it
         const int st = it % STAGES;
         if (!mbar_wait_backoff(bar.staged(st), (it / STAGES) & 1, wc)) break;
-        tma_reduce_add_3d(&tmdq, sStage + st * STAGE_BYTES, 0, (t_lo + it) * BM, bh);
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b)
+          tma_reduce_add_3d(&tmdq, sStage + st * STAGE_BYTES + b * DQ_BOX_BYTES, 32 * b, (t_lo + it) * BM, bh);
         bulk_commit_group();
         if (loaded < nsteps) {
           bulk_wait_read_all();
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       constexpr uint32_t id_kb = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (TMEM), B MN-major
-      constexpr uint32_t id_mm = idesc_bf16_f32(128, 128, 1, 1);  // both MN-major
+      constexpr uint32_t id_mm = idesc_bf16_f32(128, 128, 1, 1);  // both MN-major (dS^T, K)
       auto issue_s_dp = [&](int i) {  // S^T_i = K Q_i^T, dP^T_i = V dO_i^T
         const uint32_t qb = sStage + (i % STAGES) * STAGE_BYTES;
 #pragma unroll
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_bf16_ts(tmem + TM_DV, tmem + TM_S + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
                       sdesc_sw128(qb + TILE_BYTES + kk * 2048, BOX_BYTES, 1024), id_kb, (i > 0 || kk > 0));
-        // dK += dS^T Q_i  ;  dQ^T = K^T dS^T  (over the S^T / P^T columns, after dV read P^T)
+        // dK += dS^T Q_i  ;  dQ = dS K  (over the S^T / P^T columns, after dV read P^T)
         if (!mbar_wait(bar.ds_full(), ph, wc)) break;
         tc_fence_after();
 #pragma unroll
@@ -342,10 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(qb + kk * 2048, BOX_BYTES, 1024), id_kb, (i > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ss(tmem + TM_S, sdesc_sw128(sK + kk * 2048, BOX_BYTES, 1024),
-                      sdesc_sw128(sDS + kk * 2048, BOX_BYTES, 1024), id_mm, kk > 0);
+          mma_bf16_ss(tmem + TM_S, sdesc_sw128(sDS + kk * 2048, BOX_BYTES, 1024),
+                      sdesc_sw128(sK + kk * 2048, BOX_BYTES, 1024), id_mm, kk > 0);
         mma_commit(bar.dq_full());
-        // next tile's S^T and dP^T once dQ^T has been read out of the S^T columns
+        // next tile's S^T and dP^T once dQ has been read out of the S^T columns
         if (i + 1 < nsteps) {
           if (!mbar_wait(bar.dq_free(), ph, wc)) break;
           if (!mbar_wait(bar.q_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)) break;
@@ -454,9 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_full());
 
-      // ---- dQ^T read-out (thread = head-dimension index), staged as fp32
-      //      [query][d] in stage i%2 (its Q_i / dO_i were last read by dK_i and
-      //      dV_i, both complete once dQ^T is), for the producer's TMA reduction
+      // ---- dQ read-out (thread = query row; this warpgroup's 64 columns of d),
+      //      staged as fp32 in stage i%2 (its Q_i / dO_i were last read by dK_i
+      //      and dV_i, both complete once dQ is) as 128-byte-swizzled
+      //      [128 queries][32 d] boxes for the producer's TMA reductions
       if (!warp_wait(bar.dq_full(), ph)) {
         ok = false;
         break;
@@ -469,9 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.dq_free());
-      float* stg = reinterpret_cast<float*>(smem + OFF_STAGE + st * STAGE_BYTES) + (64 * g) * D + row;
+      {
+        const uint32_t stg = sStage + st * STAGE_BYTES + (2 * g) * DQ_BOX_BYTES + row * 128;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) stg[c * D] = __uint_as_float(qv[c]);
+        for (int c4 = 0; c4 < 16; ++c4) {  // 16-byte chunk c4 of this row's 64 values
+          const uint32_t box = c4 >> 3, chunk = c4 & 7;
+          st_shared_v4(stg + box * DQ_BOX_BYTES + ((chunk ^ (row & 7)) << 4), qv[4 * c4], qv[4 * c4 + 1],
+                       qv[4 * c4 + 2], qv[4 * c4 + 3]);
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.staged(st));

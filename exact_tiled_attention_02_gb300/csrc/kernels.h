@@ -57,7 +57,7 @@ struct FwdMaps {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO;
-  CUtensorMap dq_acc;  // fp32 [BH, N, d] accumulator: dims (d, N, BH), box (d, 128, 1), no swizzle
+  CUtensorMap dq_acc;  // fp32 [BH, N, d] accumulator: dims (d, N, BH), box (32, 128, 1), 128-byte swizzle
 };
 
 // Launchers (each returns the launch's cudaError_t).
