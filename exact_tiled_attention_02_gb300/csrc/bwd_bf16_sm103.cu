@@ -1,5 +1,5 @@
 // bwd_bf16_sm103.cu -- exact attention backward by recomputation for GB300
-// (sm_103a), bf16 in / fp32 accumulate, d = 128.
+// (sm_103a), bf16 in / fp32 accumulate, head dimension d = 64 or 128.
 //
 // "Flash attention and efficient attention -- Hinglish notes", "Backward Pass:
 // Recomputation": the N x N matrices S and P are not stored by the forward and
@@ -63,33 +63,41 @@ using namespace sm103;
 
 constexpr int BM = 128;    // query rows per step
 constexpr int BN = 128;    // keys per CTA
-constexpr int D = 128;     // head dimension
-constexpr int STAGES = 2;  // Q/dO/lse/D ring depth
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
-
-constexpr int TILE_BYTES = 128 * D * 2;   // 32 KB: a bf16 [128 x 128] tile as two 64-column boxes
-constexpr int BOX_BYTES = 128 * 128;      // 16 KB: one [128 rows x 64 cols] box
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256;  // dK follows dV
+constexpr int BOX_BYTES = 128 * 128;      // 16 KB: one bf16 [128 rows x 64 cols] box
 constexpr int VEC_BYTES = BM * 4;         // 512 B of lse*log2e or of D
 constexpr int DQ_BOX_BYTES = BM * 32 * 4; // 16 KB: fp32 dQ staging box [128 queries][32 d], 128-byte swizzled
-// 1024-aligned region: K, V, stage 0 (Q, dO), stage 1 (Q, dO), dS^T; then the
-// small items (per-stage lse2 / D vectors, barriers, tmem slot, abort flag)
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + TILE_BYTES;
-constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
-constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
-constexpr int OFF_VEC = OFF_DST + TILE_BYTES;
-constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
-// kv_full, q_full[2], staged[2], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done
-constexpr int NBAR = 1 + 2 * STAGES + 9;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_BYTES = 227 * 1024;  // the whole opt-in budget; the kernel checks the alignment pad fits
-constexpr int kMaxPad = SMEM_BYTES - SMEM_USED;
-static_assert(kMaxPad >= 0, "shared memory budget");
+constexpr int DST_BYTES = BN * BM * 2;    // 32 KB: bf16 dS^T [128 keys][128 queries] as two boxes
 
+template <int D>
+struct Cfg {
+  static constexpr int STAGES = (D == 128) ? 2 : 3;  // Q/dO/lse/D ring depth
+  static constexpr int BOXES = D / 64;               // 64-column boxes per row of a Q / K / V / dO tile
+  static constexpr int TILE_BYTES = 128 * D * 2;     // a bf16 [128 x D] tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // Q_i then dO_i; also holds the fp32 [128 x D] dQ staging
+  static constexpr uint32_t TM_DK = TM_DV + D;
+  // 1024-aligned region: K, V, the stages, dS^T; then the small items
+  // (per-stage lse2 / D vectors, barriers, tmem slot, abort flag)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE_BYTES;
+  static constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
+  static constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int OFF_VEC = OFF_DST + DST_BYTES;
+  static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
+  // kv_full, q_full[S], staged[S], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done
+  static constexpr int NBAR = 1 + 2 * STAGES + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 227 * 1024) ? SMEM_USED + 1024 : 227 * 1024;
+  static constexpr int kMaxPad = SMEM_BYTES - SMEM_USED;  // the kernel checks the alignment pad fits
+  static_assert(kMaxPad >= 0, "shared memory budget");
+  static_assert(STAGE_BYTES == BM * D * 4, "a stage holds exactly the fp32 dQ staging tile");
+  static_assert(TM_DK + D <= kTmemCols, "tensor memory budget");
+};
+
+template <int STAGES>
 struct Bars {
   uint32_t base;
   __device__ uint32_t kv_full() const { return base; }
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   }
   const long long src = (bh * N + i) * d;
   float acc = 0.f;
-  // d = 128: each lane reads 4 consecutive bf16 (8 bytes) of O and dO
+  // each pass: lane l reads 4 consecutive bf16 (8 bytes) of O and dO at column 4l
   for (int c = lane * 4; c < d; c += 128) {
     const uint2 ov = *reinterpret_cast<const uint2*>(o + src + c);
     const uint2 gv = *reinterpret_cast<const uint2*>(dO + src + c);
@@ -175,24 +183,29 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
 // ---------------------------------------------------------------------------
 // bwd_main
 // ---------------------------------------------------------------------------
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                              const __grid_constant__ CUtensorMap tmdq, const BwdParams p) {
+  using C = Cfg<D>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int TILE_BYTES = C::TILE_BYTES, STAGE_BYTES = C::STAGE_BYTES;
+  constexpr uint32_t TM_DK = C::TM_DK;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  if (pad > static_cast<uint32_t>(kMaxPad)) {
+  if (pad > static_cast<uint32_t>(C::kMaxPad)) {
     // cannot happen with a 1024-aligned dynamic shared memory base; refuse rather than overrun
     if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
     return;
   }
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sK = sb + OFF_K, sV = sb + OFF_V, sStage = sb + OFF_STAGE, sDS = sb + OFF_DST, sVec = sb + OFF_VEC;
-  const Bars bar{sb + OFF_BAR};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sStage = sb + C::OFF_STAGE, sDS = sb + C::OFF_DST, sVec = sb + C::OFF_VEC;
+  const Bars<STAGES> bar{sb + C::OFF_BAR};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const WaitCtl wc{p.status, abort_flag, p.wait_ns};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tmdo);
       prefetch_tensormap(&tmdq);
       mbar_arrive_expect_tx(bar.kv_full(), 2 * TILE_BYTES);
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < C::BOXES; ++b) {
         tma_load_3d(sK + b * BOX_BYTES, &tmk, bar.kv_full(), b * 64, k0, bh);
         tma_load_3d(sV + b * BOX_BYTES, &tmv, bar.kv_full(), b * 64, k0, bh);
       }
@@ -263,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t base = sStage + st * STAGE_BYTES;
         const uint32_t vec = sVec + st * 2 * VEC_BYTES;
         mbar_arrive_expect_tx(bar.q_full(st), STAGE_BYTES + 2 * VEC_BYTES);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::BOXES; ++b) {
           tma_load_3d(base + b * BOX_BYTES, &tmq, bar.q_full(st), b * 64, q0, bh);
           tma_load_3d(base + TILE_BYTES + b * BOX_BYTES, &tmdo, bar.q_full(st), b * 64, q0, bh);
         }
@@ -302,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
-      constexpr uint32_t id_kb = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (TMEM), B MN-major
-      constexpr uint32_t id_mm = idesc_bf16_f32(128, 128, 1, 1);  // both MN-major (dS^T, K)
+      constexpr uint32_t id_kb = idesc_bf16_f32(128, D, 0, 1);  // A K-major (TMEM), B MN-major, N = d
+      constexpr uint32_t id_mm = idesc_bf16_f32(128, D, 1, 1);  // both MN-major (dS^T, K), N = d
       auto issue_s_dp = [&](int i) {  // S^T_i = K Q_i^T, dP^T_i = V dO_i^T
         const uint32_t qb = sStage + (i % STAGES) * STAGE_BYTES;
 #pragma unroll
@@ -388,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_32x32b_x32(tS, &sv[0]);
       tmem_ld_32x32b_x32(tS + 32, &sv[32]);
       tmem_wait_ld();
-      const float4* nlse4 = reinterpret_cast<const float4*>(smem + OFF_VEC + st * 2 * VEC_BYTES + 64 * 4 * g);
-      const float4* nd4 = reinterpret_cast<const float4*>(smem + OFF_VEC + st * 2 * VEC_BYTES + VEC_BYTES + 64 * 4 * g);
+      const float4* nlse4 = reinterpret_cast<const float4*>(smem + C::OFF_VEC + st * 2 * VEC_BYTES + 64 * 4 * g);
+      const float4* nd4 = reinterpret_cast<const float4*>(smem + C::OFF_VEC + st * 2 * VEC_BYTES + VEC_BYTES + 64 * 4 * g);
       float pr[64];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
@@ -457,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_full());
 
-      // ---- dQ read-out (thread = query row; this warpgroup's 64 columns of d),
+      // ---- dQ read-out (thread = query row; this warpgroup's D/2 columns of d),
       //      staged as fp32 in stage i%2 (its Q_i / dO_i were last read by dK_i
       //      and dV_i, both complete once dQ is) as 128-byte-swizzled
       //      [128 queries][32 d] boxes for the producer's TMA reductions
@@ -466,18 +479,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t qv[64];
-      tmem_ld_32x32b_x32(tS, &qv[0]);
-      tmem_ld_32x32b_x32(tS + 32, &qv[32]);
+      constexpr int HALF = D / 2;  // d columns of this warpgroup
+      uint32_t qv[HALF];
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c) tmem_ld_32x32b_x32(tl + TM_S + g * HALF + 32 * c, &qv[32 * c]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.dq_free());
       {
-        const uint32_t stg = sStage + st * STAGE_BYTES + (2 * g) * DQ_BOX_BYTES + row * 128;
+        const uint32_t stg = sStage + st * STAGE_BYTES + row * 128;
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {  // 16-byte chunk c4 of this row's 64 values
-          const uint32_t box = c4 >> 3, chunk = c4 & 7;
+        for (int c4 = 0; c4 < HALF / 4; ++c4) {  // 16-byte chunk c4 of this row's HALF values
+          const int col = g * HALF + 4 * c4;      // first d column of the chunk
+          const uint32_t box = col >> 5, chunk = (col & 31) >> 2;
           st_shared_v4(stg + box * DQ_BOX_BYTES + ((chunk ^ (row & 7)) << 4), qv[4 * c4], qv[4 * c4 + 1],
                        qv[4 * c4 + 2], qv[4 * c4 + 3]);
         }
@@ -489,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ epilogue
     // warpgroup 0 writes dV, warpgroup 1 writes scale * dK, each staged as a
-    // bf16 [128 keys][128 d] tile in an idle Q/dO stage
+    // bf16 [128 keys][D] tile in an idle Q/dO stage
     const bool have = ok && warp_wait(bar.fin(), 0) && warp_wait(bar.prod_done(), 0);
     const uint32_t stage_out = sStage + g * STAGE_BYTES;
     if (have) {
@@ -508,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * mul, __uint_as_float(v[q4 * 8 + 2 * e + 1]) * mul);
-          // row-major [128 keys][128 d] bf16 with 16-byte chunks swizzled by row
-          st_shared_v4(stage_out + row * 256 + ((c16 ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+          // row-major [128 keys][D] bf16 with 16-byte chunks swizzled by row
+          st_shared_v4(stage_out + row * (2 * D) + ((c16 ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
         }
       }
     }
@@ -517,11 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(1 + g, 128);
     if (have && !*abort_flag) {
       uint8_t* gout = reinterpret_cast<uint8_t*>(g == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * N + k0) * D * 2;
-      for (int idx = row; idx < BN * 16; idx += 128) {
-        const int rr = idx >> 4, c16 = idx & 15;
+      constexpr int CHUNKS = D / 8;
+      for (int idx = row; idx < BN * CHUNKS; idx += 128) {
+        const int rr = idx / CHUNKS, c16 = idx % CHUNKS;
         if (k0 + rr < N)
-          st_global_v4(gout + static_cast<size_t>(rr) * 256 + c16 * 16,
-                       ld_shared_v4(stage_out + rr * 256 + ((c16 ^ (rr & 7)) << 4)));
+          st_global_v4(gout + static_cast<size_t>(rr) * (2 * D) + c16 * 16,
+                       ld_shared_v4(stage_out + rr * (2 * D) + ((c16 ^ (rr & 7)) << 4)));
       }
     }
   }
@@ -546,15 +562,25 @@ size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_
   return acc + 2 * vec;
 }
 
-cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s) {
-  if (p.d != D) return cudaErrorNotSupported;
+namespace {
+
+template <int D>
+cudaError_t launch_main(const BwdParams& p, const BwdMaps& m, unsigned grid, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_bf16_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_bf16_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  fa_bwd_bf16_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, m.dq_acc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s) {
+  if (p.d != 128 && p.d != 64) return cudaErrorNotSupported;
   const long long np = npad128(p.N);
   const long long prep_rows = static_cast<long long>(p.BH) * np;
   const long long prep_blocks = (prep_rows + 7) / 8;
@@ -568,8 +594,8 @@ cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_
       p.dq_acc, p.BH, p.N, p.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_bf16_sm103_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, m.dq_acc, p);
-  e = cudaGetLastError();
+  e = p.d == 128 ? launch_main<128>(p, m, static_cast<unsigned>(grid), s)
+                 : launch_main<64>(p, m, static_cast<unsigned>(grid), s);
   if (e != cudaSuccess) return e;
   fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
       p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8, p.scale);

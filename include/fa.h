@@ -101,7 +101,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                    owned by the caller, 256-byte aligned; its contents on
  *                    entry do not matter and are undefined on return.
  *   workspace_bytes  its size; smaller than required -> FA_ERR_INVALID.
- * bf16 with d = 128 only in this version; other d and FA_DTYPE_F32 return
+ * bf16 with d = 64 or 128; other d and FA_DTYPE_F32 return
  * FA_ERR_UNSUPPORTED.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -70,6 +70,11 @@ BWD_CASES = [
     (1, 1, 700, 128, 65, 1.0),
     (1, 1, 1000, 128, 257, 1.0),
     (1, 1, 640, 128, 257, 8.0),
+    (1, 1, 1, 64, 0, 1.0),
+    (1, 2, 65, 64, 0, 1.0),
+    (2, 2, 300, 64, 0, 8.0),
+    (1, 1, 513, 64, 0, 1.0),
+    (1, 2, 700, 64, 65, 1.0),
 ]
 
 
@@ -93,6 +98,17 @@ def test_bwd_deterministic_dk_dv():
     b = _run(q, k, v, do, 1 / np.sqrt(128), 0, dev)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert _rel(_np(a[0]), _np(b[0])) <= 1e-3
+
+
+def test_bwd_d64_large_sampled_heads():
+    """d = 64 at a size with many key and query tiles (B=2, H=8, N=2048)."""
+    dev = _dev()
+    q, k, v, do = inputs.make_inputs(2, 8, 2048, 64, "bf16", seed=64, with_do=True)
+    dq, dk, dv = _run(q, k, v, do, 0.125, 0, dev)
+    for b, h in ((0, 0), (1, 7)):
+        refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), 0.125)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
+            assert _rel(_np(g), r) <= 1e-2, (name, b, h, _rel(_np(g), r))
 
 
 def test_workload5_full_size_sampled_heads():
@@ -122,11 +138,11 @@ def test_workload5_full_size_sampled_heads():
 def test_bwd_unsupported_requests():
     dev = _dev()
     fa = _fa()
-    x = torch.zeros(1, 1, 8, 64, device=dev, dtype=torch.bfloat16)
+    x = torch.zeros(1, 1, 8, 96, device=dev, dtype=torch.bfloat16)
     lse = torch.zeros(1, 1, 8, device=dev, dtype=torch.float32)
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(x, x, x, x, lse, x)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # bf16 head dimensions are 64 and 128
     y = torch.zeros(1, 1, 8, 128, device=dev, dtype=torch.float32)
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(y, y, y, y, lse, y)
