@@ -86,8 +86,9 @@ struct Cfg {
   static constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
   static constexpr int OFF_VEC = OFF_DST + DST_BYTES;
   static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
-  // kv_full, q_full[S], staged[S], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done
-  static constexpr int NBAR = 1 + 2 * STAGES + 9;
+  // kv_full, q_full[S], staged[S], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done,
+  // dk_done
+  static constexpr int NBAR = 1 + 2 * STAGES + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 227 * 1024) ? SMEM_USED + 1024 : 227 * 1024;
@@ -112,6 +113,7 @@ struct Bars {
   __device__ uint32_t fin() const { return base + 8 * (7 + 2 * STAGES); }
   __device__ uint32_t drain() const { return base + 8 * (8 + 2 * STAGES); }
   __device__ uint32_t prod_done() const { return base + 8 * (9 + 2 * STAGES); }
+  __device__ uint32_t dk_done() const { return base + 8 * (10 + 2 * STAGES); }
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.fin(), 1);
     mbar_init(bar.drain(), 1);
     mbar_init(bar.prod_done(), 1);
+    mbar_init(bar.dk_done(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -349,18 +352,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_bf16_ts(tmem + TM_DV, tmem + TM_S + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
                       sdesc_sw128(qb + TILE_BYTES + kk * 2048, BOX_BYTES, 1024), id_kb, (i > 0 || kk > 0));
-        // dK += dS^T Q_i  ;  dQ = dS K  (over the S^T / P^T columns, after dV read P^T)
+        // dQ = dS K first (over the S^T / P^T columns, after dV read P^T), so the
+        // warpgroups can read dQ and free those columns while dK += dS^T Q_i runs
         if (!mbar_wait(bar.ds_full(), ph, wc)) break;
         tc_fence_after();
+        const uint32_t dsb = sDS;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ss(tmem + TM_S, sdesc_sw128(dsb + kk * 2048, BOX_BYTES, 1024),
+                      sdesc_sw128(sK + kk * 2048, BOX_BYTES, 1024), id_mm, kk > 0);
+        mma_commit(bar.dq_full());
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_bf16_ts(tmem + TM_DK, tmem + TM_DP + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
                       sdesc_sw128(qb + kk * 2048, BOX_BYTES, 1024), id_kb, (i > 0 || kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ss(tmem + TM_S, sdesc_sw128(sDS + kk * 2048, BOX_BYTES, 1024),
-                      sdesc_sw128(sK + kk * 2048, BOX_BYTES, 1024), id_mm, kk > 0);
-        mma_commit(bar.dq_full());
+        mma_commit(bar.dk_done());  // Q_i's last reader: its stage may take the dQ staging
         // next tile's S^T and dP^T once dQ has been read out of the S^T columns
         if (i + 1 < nsteps) {
           if (!mbar_wait(bar.dq_free(), ph, wc)) break;
@@ -471,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar.ds_full());
 
       // ---- dQ read-out (thread = query row; this warpgroup's D/2 columns of d),
-      //      staged as fp32 in stage i%2 (its Q_i / dO_i were last read by dK_i
-      //      and dV_i, both complete once dQ is) as 128-byte-swizzled
+      //      staged as fp32 in stage i%2 (its dO_i was last read by dV_i, done
+      //      once dQ is; its Q_i by dK_i, awaited below) as 128-byte-swizzled
       //      [128 queries][32 d] boxes for the producer's TMA reductions
       if (!warp_wait(bar.dq_full(), ph)) {
         ok = false;
@@ -487,6 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.dq_free());
+      // the stage still holds Q_i until dK_i (issued after dQ_i) has read it
+      if (!warp_wait(bar.dk_done(), ph)) {
+        ok = false;
+        break;
+      }
       {
         const uint32_t stg = sStage + st * STAGE_BYTES + row * 128;
 #pragma unroll
