@@ -86,9 +86,9 @@ struct Cfg {
   static constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
   static constexpr int OFF_VEC = OFF_DST + DST_BYTES;
   static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
-  // kv_full, q_full[S], staged[S], s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done,
-  // dk_done
-  static constexpr int NBAR = 1 + 2 * STAGES + 10;
+  // kv_full, qa_full[S] (Q + vectors), qo_full[S] (dO), staged_q[S], staged_o[S] (the two halves of the dQ
+  // staging), s_full, dp_full, p_full, ds_full, dq_full, dq_free, fin, drain, prod_done, dk_done
+  static constexpr int NBAR = 1 + 4 * STAGES + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 227 * 1024) ? SMEM_USED + 1024 : 227 * 1024;
@@ -102,18 +102,21 @@ template <int STAGES>
 struct Bars {
   uint32_t base;
   __device__ uint32_t kv_full() const { return base; }
-  __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t staged(int s) const { return base + 8 * (1 + STAGES + s); }
-  __device__ uint32_t s_full() const { return base + 8 * (1 + 2 * STAGES); }
-  __device__ uint32_t dp_full() const { return base + 8 * (2 + 2 * STAGES); }
-  __device__ uint32_t p_full() const { return base + 8 * (3 + 2 * STAGES); }
-  __device__ uint32_t ds_full() const { return base + 8 * (4 + 2 * STAGES); }
-  __device__ uint32_t dq_full() const { return base + 8 * (5 + 2 * STAGES); }
-  __device__ uint32_t dq_free() const { return base + 8 * (6 + 2 * STAGES); }
-  __device__ uint32_t fin() const { return base + 8 * (7 + 2 * STAGES); }
-  __device__ uint32_t drain() const { return base + 8 * (8 + 2 * STAGES); }
-  __device__ uint32_t prod_done() const { return base + 8 * (9 + 2 * STAGES); }
-  __device__ uint32_t dk_done() const { return base + 8 * (10 + 2 * STAGES); }
+  __device__ uint32_t qa_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t qo_full(int s) const { return base + 8 * (1 + STAGES + s); }
+  __device__ uint32_t staged_q(int s) const { return base + 8 * (1 + 2 * STAGES + s); }
+  __device__ uint32_t staged_o(int s) const { return base + 8 * (1 + 3 * STAGES + s); }
+  __device__ uint32_t at(int k) const { return base + 8 * (1 + 4 * STAGES + k); }
+  __device__ uint32_t s_full() const { return at(0); }
+  __device__ uint32_t dp_full() const { return at(1); }
+  __device__ uint32_t p_full() const { return at(2); }
+  __device__ uint32_t ds_full() const { return at(3); }
+  __device__ uint32_t dq_full() const { return at(4); }
+  __device__ uint32_t dq_free() const { return at(5); }
+  __device__ uint32_t fin() const { return at(6); }
+  __device__ uint32_t drain() const { return at(7); }
+  __device__ uint32_t prod_done() const { return at(8); }
+  __device__ uint32_t dk_done() const { return at(9); }
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
@@ -228,8 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar.kv_full(), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar.q_full(s), 1);
-      mbar_init(bar.staged(s), 8);  // one arrive per compute warp
+      mbar_init(bar.qa_full(s), 1);
+      mbar_init(bar.qo_full(s), 1);
+      mbar_init(bar.staged_q(s), 4);  // one arrive per warp of compute warpgroup 0
+      mbar_init(bar.staged_o(s), 4);  // ... of compute warpgroup 1
     }
     mbar_init(bar.s_full(), 1);
     mbar_init(bar.dp_full(), 1);
@@ -273,34 +278,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sK + b * BOX_BYTES, &tmk, bar.kv_full(), b * 64, k0, bh);
         tma_load_3d(sV + b * BOX_BYTES, &tmv, bar.kv_full(), b * 64, k0, bh);
       }
-      auto load = [&](int it) {
+      // tile `it` into stage it % STAGES, in two parts: Q_it with the lse / D
+      // vectors, and dO_it (each part reuses the stage half that the dQ
+      // staging of tile it - STAGES occupied)
+      auto load_q = [&](int it) {
         const int st = it % STAGES;
         const int q0 = (t_lo + it) * BM;
         const uint32_t base = sStage + st * STAGE_BYTES;
         const uint32_t vec = sVec + st * 2 * VEC_BYTES;
-        mbar_arrive_expect_tx(bar.q_full(st), STAGE_BYTES + 2 * VEC_BYTES);
-        for (int b = 0; b < C::BOXES; ++b) {
-          tma_load_3d(base + b * BOX_BYTES, &tmq, bar.q_full(st), b * 64, q0, bh);
-          tma_load_3d(base + TILE_BYTES + b * BOX_BYTES, &tmdo, bar.q_full(st), b * 64, q0, bh);
-        }
+        mbar_arrive_expect_tx(bar.qa_full(st), TILE_BYTES + 2 * VEC_BYTES);
+        for (int b = 0; b < C::BOXES; ++b) tma_load_3d(base + b * BOX_BYTES, &tmq, bar.qa_full(st), b * 64, q0, bh);
         const size_t vrow = static_cast<size_t>(bh) * np + q0;
-        bulk_load(vec, p.lse2 + vrow, VEC_BYTES, bar.q_full(st));
-        bulk_load(vec + VEC_BYTES, p.dsum + vrow, VEC_BYTES, bar.q_full(st));
+        bulk_load(vec, p.lse2 + vrow, VEC_BYTES, bar.qa_full(st));
+        bulk_load(vec + VEC_BYTES, p.dsum + vrow, VEC_BYTES, bar.qa_full(st));
+      };
+      auto load_o = [&](int it) {
+        const int st = it % STAGES;
+        const int q0 = (t_lo + it) * BM;
+        const uint32_t base = sStage + st * STAGE_BYTES + TILE_BYTES;
+        mbar_arrive_expect_tx(bar.qo_full(st), TILE_BYTES);
+        for (int b = 0; b < C::BOXES; ++b) tma_load_3d(base + b * BOX_BYTES, &tmdo, bar.qo_full(st), b * 64, q0, bh);
       };
       int loaded = 0;
-      for (; loaded < STAGES && loaded < nsteps; ++loaded) load(loaded);
+      for (; loaded < STAGES && loaded < nsteps; ++loaded) {
+        load_q(loaded);
+        load_o(loaded);
+      }
+      constexpr int HALF_BOXES = D / 64;  // fp32 staging boxes per half (per compute warpgroup)
       for (int it = 0; it < nsteps; ++it) {
-        // tile it's dQ^T is staged in stage it%2: reduce it into the accumulator,
-        // then reuse the stage for tile it+2 once the reduction has read it
+        // tile it's dQ is staged in stage it % STAGES: warpgroup 0's columns over
+        // the Q half, warpgroup 1's over the dO half.  Reduce the Q half first
+        // and reload Q (which the next tile's first product needs) as soon as
+        // that half has been read, then the dO half.
         const int st = it % STAGES;
-        if (!mbar_wait_backoff(bar.staged(st), (it / STAGES) & 1, wc)) break;
+        const uint32_t sbase = sStage + st * STAGE_BYTES;
+        const int q0 = (t_lo + it) * BM;
+        if (!mbar_wait_backoff(bar.staged_q(st), (it / STAGES) & 1, wc)) break;
 #pragma unroll
-        for (int b = 0; b < D / 32; ++b)
-          tma_reduce_add_3d(&tmdq, sStage + st * STAGE_BYTES + b * DQ_BOX_BYTES, 32 * b, (t_lo + it) * BM, bh);
+        for (int b = 0; b < HALF_BOXES; ++b)
+          tma_reduce_add_3d(&tmdq, sbase + b * DQ_BOX_BYTES, 32 * b, q0, bh);
+        bulk_commit_group();
+        if (!mbar_wait_backoff(bar.staged_o(st), (it / STAGES) & 1, wc)) break;
+#pragma unroll
+        for (int b = HALF_BOXES; b < 2 * HALF_BOXES; ++b)
+          tma_reduce_add_3d(&tmdq, sbase + b * DQ_BOX_BYTES, 32 * b, q0, bh);
         bulk_commit_group();
         if (loaded < nsteps) {
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the Q half has been read
+          load_q(loaded);
           bulk_wait_read_all();
-          load(loaded);
+          load_o(loaded);
           ++loaded;
         }
       }
@@ -308,8 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) {
         WaitCtl drain{nullptr, nullptr, wc.limit_ns};
         mbar_wait(bar.kv_full(), 0, drain);
-        for (int it = max(0, loaded - STAGES); it < loaded; ++it)
-          mbar_wait(bar.q_full(it % STAGES), (it / STAGES) & 1, drain);
+        for (int it = max(0, loaded - STAGES); it < loaded; ++it) {
+          mbar_wait(bar.qa_full(it % STAGES), (it / STAGES) & 1, drain);
+          mbar_wait(bar.qo_full(it % STAGES), (it / STAGES) & 1, drain);
+        }
       }
       mbar_arrive(bar.prod_done());
     }
@@ -320,14 +349,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       constexpr uint32_t id_kb = idesc_bf16_f32(128, D, 0, 1);  // A K-major (TMEM), B MN-major, N = d
       constexpr uint32_t id_mm = idesc_bf16_f32(128, D, 1, 1);  // both MN-major (dS^T, K), N = d
-      auto issue_s_dp = [&](int i) {  // S^T_i = K Q_i^T, dP^T_i = V dO_i^T
-        const uint32_t qb = sStage + (i % STAGES) * STAGE_BYTES;
+      // S^T_i = K Q_i^T, then dP^T_i = V dO_i^T, each once its operand tile is resident
+      auto issue_s_dp = [&](int i) -> bool {
+        const int st = i % STAGES;
+        const uint32_t qb = sStage + st * STAGE_BYTES;
+        if (!mbar_wait(bar.qa_full(st), (i / STAGES) & 1, wc)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
           mma_bf16_ss(tmem + TM_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), id_kk, kk > 0);
         }
         mma_commit(bar.s_full());
+        if (!mbar_wait(bar.qo_full(st), (i / STAGES) & 1, wc)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
@@ -335,12 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       id_kk, kk > 0);
         }
         mma_commit(bar.dp_full());
+        return true;
       };
-      bool ok = mbar_wait(bar.kv_full(), 0, wc) && mbar_wait(bar.q_full(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_s_dp(0);
-      }
+      bool ok = mbar_wait(bar.kv_full(), 0, wc) && issue_s_dp(0);
       for (int i = 0; ok && i < nsteps; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = i & 1;
@@ -370,9 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next tile's S^T and dP^T once dQ has been read out of the S^T columns
         if (i + 1 < nsteps) {
           if (!mbar_wait(bar.dq_free(), ph, wc)) break;
-          if (!mbar_wait(bar.q_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)) break;
-          tc_fence_after();
-          issue_s_dp(i + 1);
+          if (!issue_s_dp(i + 1)) break;
         }
       }
       mma_commit(bar.fin());
@@ -398,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i % STAGES;
       const int q0 = (t_lo + i) * BM + 64 * g;  // first query column of this warpgroup
       // ---- P^T = exp2(S^T * scale * log2e - lse * log2e)
-      if (!warp_wait(bar.s_full(), ph) || !warp_wait(bar.q_full(st), (i / STAGES) & 1)) {
+      if (!warp_wait(bar.s_full(), ph) || !warp_wait(bar.qa_full(st), (i / STAGES) & 1)) {
         ok = false;
         break;
       }
@@ -477,9 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar.ds_full());
 
       // ---- dQ read-out (thread = query row; this warpgroup's D/2 columns of d),
-      //      staged as fp32 in stage i%2 (its dO_i was last read by dV_i, done
-      //      once dQ is; its Q_i by dK_i, awaited below) as 128-byte-swizzled
-      //      [128 queries][32 d] boxes for the producer's TMA reductions
+      //      staged as fp32 in stage i % STAGES as 128-byte-swizzled [128 queries]
+      //      [32 d] boxes for the producer's TMA reductions: warpgroup g's boxes
+      //      cover stage half g (half 0 held Q_i, half 1 held dO_i)
       if (!warp_wait(bar.dq_full(), ph)) {
         ok = false;
         break;
@@ -493,8 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.dq_free());
-      // the stage still holds Q_i until dK_i (issued after dQ_i) has read it
-      if (!warp_wait(bar.dk_done(), ph)) {
+      // warpgroup 0 stages over Q_i, which dK_i (issued after dQ_i) may still be
+      // reading; warpgroup 1 stages over dO_i, last read by dV_i (before dQ_i)
+      if (g == 0 && !warp_wait(bar.dk_done(), ph)) {
         ok = false;
         break;
       }
@@ -510,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.staged(st));
+      if (lane == 0) mbar_arrive(g == 0 ? bar.staged_q(st) : bar.staged_o(st));
     }
 
     // ------------------------------------------------------------ epilogue
