@@ -220,7 +220,6 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   const fa_status c = check_common(B, H, N, d, scale, window, dt);
   if (c != FA_OK) return c;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
-  if (dt != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
 
   BwdParams p{};
   p.q = q;
@@ -246,6 +245,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.wait_ns = wait_ns();
   if (status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (dt == FA_DTYPE_F32) return launch_bwd_f32_simt(p, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 
   BwdMaps m;
   if (!make_map_bf16(&m.q, q, p.BH, N, d, kBwdBlockRows) || !make_map_bf16(&m.k, k, p.BH, N, d, kBwdBlockCols) ||

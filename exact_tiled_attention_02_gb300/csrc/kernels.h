@@ -64,6 +64,7 @@ struct BwdMaps {
 cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
+cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
 // Byte size of the backward workspace and the offsets of its lse2 / dsum
 // sections (dq_acc is at offset 0); rows are padded to multiples of 128.
 size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum);

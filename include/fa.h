@@ -27,7 +27,7 @@
  *            fp32-accumulated tensor-core math with P rounded to bf16 before
  *            the P V product; d must be 64 or 128.
  *            FA_DTYPE_F32: all arrays are float32 and all arithmetic is exact
- *            fp32 on CUDA cores; 1 <= d <= 128 (forward only in this version).
+ *            fp32 on CUDA cores with the accurate expf/logf; 1 <= d <= 128.
  * scale      finite and > 0; usually 1/sqrt(d).
  * window     <= 0: unmasked.  Otherwise an odd full width w; r = (w - 1) / 2.
  *            Even widths are rejected (the pages give them no meaning).
@@ -101,8 +101,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                    owned by the caller, 256-byte aligned; its contents on
  *                    entry do not matter and are undefined on return.
  *   workspace_bytes  its size; smaller than required -> FA_ERR_INVALID.
- * bf16 with d = 64 or 128; other d and FA_DTYPE_F32 return
- * FA_ERR_UNSUPPORTED.
+ * bf16 with d = 64 or 128 (other d return FA_ERR_UNSUPPORTED), or float32
+ * with 1 <= d <= 128 (CUDA cores; one warp per query row for dQ and one per
+ * key row for dK and dV, so dK and dV need no atomics and the float32 path
+ * is bitwise repeatable).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dO, void* dq, void* dk, void* dv,

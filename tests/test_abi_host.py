@@ -87,7 +87,7 @@ def test_fwd_rejects_on_host(b, kw, code):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=0), 1), (dict(ws=P + 16), 1), (dict(ws_bytes=100), 1), (dict(lse=0), 1),
-    (dict(window=2), 1), (dict(scale=0.0), 1), (dict(d=96), 2), (dict(d=32), 2), (dict(dt=0, d=64), 2),
+    (dict(window=2), 1), (dict(scale=0.0), 1), (dict(d=96), 2), (dict(d=32), 2), (dict(dt=0, d=129), 2),
 ])
 def test_bwd_rejects_on_host(b, kw, code):
     assert bwd(b, **kw) == code

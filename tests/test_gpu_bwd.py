@@ -143,7 +143,52 @@ def test_bwd_unsupported_requests():
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(x, x, x, x, lse, x)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED  # bf16 head dimensions are 64 and 128
-    y = torch.zeros(1, 1, 8, 128, device=dev, dtype=torch.float32)
+    y = torch.zeros(1, 1, 8, 132, device=dev, dtype=torch.float32)
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(y, y, y, y, lse, y)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # float32 head dimensions are 1..128
+
+
+# float32 backward (CUDA cores, accurate expf).  Each gradient element is a
+# sum of at most N + d fp32 products, so its rounding error is of the order
+# sqrt(N + d) * 2^-24 relative to the sum of the magnitudes (worst case
+# (N + d) * 2^-24 = 6e-5 at N + d = 1000).  Bar: relative L2 <= 2e-5 per
+# gradient; an exactly zero gradient (N = 1) within 1e-6 absolute.
+F32_BWD_CASES = [
+    # B, H, N, d, window
+    (1, 1, 1, 4, 0), (1, 2, 5, 4, 0), (2, 1, 33, 17, 0), (1, 3, 100, 64, 0), (1, 1, 77, 128, 0),
+    (1, 2, 50, 8, 3), (1, 1, 200, 32, 65), (2, 2, 129, 4, 257), (1, 1, 600, 128, 0),
+]
+
+
+def _check_f32_grad(name, g, r, what):
+    assert np.all(np.isfinite(g)), (name, what)
+    if np.linalg.norm(r) == 0.0:
+        assert np.max(np.abs(g)) <= 1e-6, (name, np.max(np.abs(g)), what)
+    else:
+        assert _rel(g, r) <= 2e-5, (name, _rel(g, r), what)
+
+
+@pytest.mark.parametrize("B,H,N,d,window", F32_BWD_CASES)
+def test_bwd_f32_elementwise(B, H, N, d, window):
+    dev = _dev()
+    q, k, v, do = inputs.make_inputs(B, H, N, d, "f32", seed=11 * N + d + window, with_do=True)
+    scale = 1 / np.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, scale, window, dev)
+    refs = oracle.dense_backward(_np(q), _np(k), _np(v), _np(do), scale, window)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        _check_f32_grad(name, _np(g), r, (B, H, N, d, window))
+
+
+def test_bwd_f32_workload1_and_repeatable():
+    """The float32 [1, 1, 6, 4] workload with a dO drawn after q, k, v from
+    the same generator; no atomics anywhere, so two runs agree bit for bit."""
+    dev = _dev()
+    w = configs.WORKLOADS[1]
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    a = _run(q, k, v, do, w.scale, w.window, dev)
+    b = _run(q, k, v, do, w.scale, w.window, dev)
+    refs = oracle.dense_backward(_np(q), _np(k), _np(v), _np(do), w.scale, w.window)
+    for name, g, g2, r in zip(("dq", "dk", "dv"), a, b, refs):
+        assert torch.equal(g, g2), name
+        assert np.abs(_np(g) - r).max() <= 1e-5, (name, np.abs(_np(g) - r).max())
