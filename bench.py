@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3, help="workload index (configs.WORKLOADS)")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d[,window[,qk_mult]]: a bf16 problem of another shape instead of a workload "
+                         "(for measuring other head dimensions; not a bench line of record)")
     ap.add_argument("--no-bwd", action="store_true", help="forward only")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -238,7 +241,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    w = configs.WORKLOADS[args.workload]
+    w = configs.WORKLOADS[args.workload] if args.shape is None else configs.custom_workload(args.shape)
 
     if args.impl == "reference":
         if rank != 0:

@@ -60,3 +60,17 @@ WORKLOADS = {
     4: Workload(4, "fwd_bf16_b1_h32_n16384_d128_w257", 1, 32, 16384, 128, "bf16", window=257),
     5: Workload(5, "bwd_bf16_b4_h16_n4096_d128", 4, 16, 4096, 128, "bf16", passes=("fwd", "bwd")),
 }
+
+
+def custom_workload(spec: str) -> Workload:
+    """A bf16 workload of another shape, from ``"B,H,N,d[,window[,qk_mult]]"``.
+    It has index 0, so its inputs are drawn with seed -1."""
+    parts = [p.strip() for p in spec.split(",")]
+    if not 4 <= len(parts) <= 6:
+        raise ValueError("shape must be B,H,N,d[,window[,qk_mult]]")
+    B, H, N, d = (int(x) for x in parts[:4])
+    window = int(parts[4]) if len(parts) > 4 else 0
+    qk = float(parts[5]) if len(parts) > 5 else 1.0
+    name = f"custom_bf16_b{B}_h{H}_n{N}_d{d}" + (f"_w{window}" if window > 0 else "") + \
+        (f"_qk{qk:g}" if qk != 1.0 else "")
+    return Workload(0, name, B, H, N, d, "bf16", window=window, qk_mult=qk, passes=("fwd", "bwd"))

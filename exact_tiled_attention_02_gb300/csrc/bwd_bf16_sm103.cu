@@ -1,5 +1,5 @@
 // bwd_bf16_sm103.cu -- exact attention backward by recomputation for GB300
-// (sm_103a), bf16 in / fp32 accumulate, head dimension d = 64 or 128.
+// (sm_103a), bf16 in / fp32 accumulate, head dimension d = 64, 96 or 128.
 //
 // "Flash attention and efficient attention -- Hinglish notes", "Backward Pass:
 // Recomputation": the N x N matrices S and P are not stored by the forward and
@@ -24,7 +24,7 @@
 //                  dQ   = dS K_j          (shared memory: dS^T and K_j read
 //                                           MN-major; TMEM lanes = queries)
 //                dV and dK accumulate in tensor memory for the whole loop; each
-//                dQ tile is staged as fp32 [128 queries][128 d] (four 128-byte-
+//                dQ tile is staged as fp32 [128 queries][d] (d / 32 128-byte-
 //                swizzled boxes of 32 columns) in the shared-memory stage its
 //                Q / dO tiles just vacated, and added to the fp32 accumulator
 //                by TMA reductions (cp.reduce.async.bulk.tensor .add.f32), so
@@ -53,6 +53,8 @@
 //   [256,384) dV      [384,512) dK
 // tcgen05.mma operations issued by one thread execute in order, so a product
 // that overwrites columns another product reads is issued after it.
+#include <type_traits>
+
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -71,13 +73,26 @@ constexpr int VEC_BYTES = BM * 4;         // 512 B of lse*log2e or of D
 constexpr int DQ_BOX_BYTES = BM * 32 * 4; // 16 KB: fp32 dQ staging box [128 queries][32 d], 128-byte swizzled
 constexpr int DST_BYTES = BN * BM * 2;    // 32 KB: bf16 dS^T [128 keys][128 queries] as two boxes
 
+// D = 64, 96 or 128.  Tiles in shared memory are DP = D rounded up to a
+// multiple of 64 columns wide (whole 128-byte swizzle atoms; for D = 96 the
+// TMA zero-fills columns 96..127).  S^T and dP^T contract over the D real
+// columns; the three products with N = d (dV, dK, dQ) run with N = DP, since a
+// 128-byte-swizzled MN-major operand is laid out in 64-column atoms: the zero
+// columns only produce zero columns, which are never read.
 template <int D>
 struct Cfg {
-  static constexpr int STAGES = (D == 128) ? 2 : 3;  // Q/dO/lse/D ring depth
-  static constexpr int BOXES = D / 64;               // 64-column boxes per row of a Q / K / V / dO tile
-  static constexpr int TILE_BYTES = 128 * D * 2;     // a bf16 [128 x D] tile
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // Q_i then dO_i; also holds the fp32 [128 x D] dQ staging
-  static constexpr uint32_t TM_DK = TM_DV + D;
+  static constexpr int DP = (D + 63) / 64 * 64;
+  static constexpr int STAGES = (DP == 128) ? 2 : 3;  // Q/dO/lse/D ring depth
+  static constexpr int BOXES = DP / 64;               // 64-column boxes per row of a Q / K / V / dO tile
+  static constexpr int TILE_BYTES = 128 * DP * 2;     // a bf16 [128 x DP] tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // Q_i then dO_i; also holds the fp32 [128 x D] dQ staging
+  // dQ staging: fp32 boxes of 32 columns; warpgroup 0 stages boxes [0, QBOXES)
+  // over the Q half of the stage, warpgroup 1 the rest over the dO half
+  static constexpr int DQ_BOXES = D / 32;
+  static constexpr int QBOXES = TILE_BYTES / DQ_BOX_BYTES;
+  static constexpr int DQ_COLS0 = 32 * QBOXES;       // d columns of warpgroup 0
+  static constexpr int DQ_COLS1 = D - DQ_COLS0;      // d columns of warpgroup 1
+  static constexpr uint32_t TM_DK = TM_DV + DP;
   // 1024-aligned region: K, V, the stages, dS^T; then the small items
   // (per-stage lse2 / D vectors, barriers, tmem slot, abort flag)
   static constexpr int OFF_K = 0;
@@ -94,8 +109,8 @@ struct Cfg {
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 227 * 1024) ? SMEM_USED + 1024 : 227 * 1024;
   static constexpr int kMaxPad = SMEM_BYTES - SMEM_USED;  // the kernel checks the alignment pad fits
   static_assert(kMaxPad >= 0, "shared memory budget");
-  static_assert(STAGE_BYTES == BM * D * 4, "a stage holds exactly the fp32 dQ staging tile");
-  static_assert(TM_DK + D <= kTmemCols, "tensor memory budget");
+  static_assert(D % 32 == 0 && DQ_COLS1 > 0 && DQ_COLS1 <= TILE_BYTES / (BM * 4), "dQ staging fits the stage");
+  static_assert(TM_DK + DP <= kTmemCols, "tensor memory budget");
 };
 
 template <int STAGES>
@@ -304,7 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_q(loaded);
         load_o(loaded);
       }
-      constexpr int HALF_BOXES = D / 64;  // fp32 staging boxes per half (per compute warpgroup)
       for (int it = 0; it < nsteps; ++it) {
         // tile it's dQ is staged in stage it % STAGES: warpgroup 0's columns over
         // the Q half, warpgroup 1's over the dO half.  Reduce the Q half first
@@ -315,12 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = (t_lo + it) * BM;
         if (!mbar_wait_backoff(bar.staged_q(st), (it / STAGES) & 1, wc)) break;
 #pragma unroll
-        for (int b = 0; b < HALF_BOXES; ++b)
+        for (int b = 0; b < C::QBOXES; ++b)
           tma_reduce_add_3d(&tmdq, sbase + b * DQ_BOX_BYTES, 32 * b, q0, bh);
         bulk_commit_group();
         if (!mbar_wait_backoff(bar.staged_o(st), (it / STAGES) & 1, wc)) break;
 #pragma unroll
-        for (int b = HALF_BOXES; b < 2 * HALF_BOXES; ++b)
+        for (int b = C::QBOXES; b < C::DQ_BOXES; ++b)
           tma_reduce_add_3d(&tmdq, sbase + b * DQ_BOX_BYTES, 32 * b, q0, bh);
         bulk_commit_group();
         if (loaded < nsteps) {
@@ -347,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
-      constexpr uint32_t id_kb = idesc_bf16_f32(128, D, 0, 1);  // A K-major (TMEM), B MN-major, N = d
-      constexpr uint32_t id_mm = idesc_bf16_f32(128, D, 1, 1);  // both MN-major (dS^T, K), N = d
+      constexpr uint32_t id_kb = idesc_bf16_f32(128, C::DP, 0, 1);  // A K-major (TMEM), B MN-major, N = DP
+      constexpr uint32_t id_mm = idesc_bf16_f32(128, C::DP, 1, 1);  // both MN-major (dS^T, K), N = DP
       // S^T_i = K Q_i^T, then dP^T_i = V dO_i^T, each once its operand tile is resident
       auto issue_s_dp = [&](int i) -> bool {
         const int st = i % STAGES;
@@ -506,38 +520,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_full());
 
-      // ---- dQ read-out (thread = query row; this warpgroup's D/2 columns of d),
-      //      staged as fp32 in stage i % STAGES as 128-byte-swizzled [128 queries]
-      //      [32 d] boxes for the producer's TMA reductions: warpgroup g's boxes
-      //      cover stage half g (half 0 held Q_i, half 1 held dO_i)
+      // ---- dQ read-out (thread = query row; warpgroup 0 takes the d columns
+      //      that fill the Q half of the stage, warpgroup 1 the rest), staged as
+      //      fp32 in stage i % STAGES as 128-byte-swizzled [128 queries][32 d]
+      //      boxes for the producer's TMA reductions (half 0 held Q_i, half 1
+      //      held dO_i)
       if (!warp_wait(bar.dq_full(), ph)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      constexpr int HALF = D / 2;  // d columns of this warpgroup
-      uint32_t qv[HALF];
+      // this warpgroup's NC d columns from col0: read out, free the columns, stage
+      auto dq_out = [&](auto nc, int col0) -> bool {
+        constexpr int NC = decltype(nc)::value;
+        uint32_t qv[NC];
 #pragma unroll
-      for (int c = 0; c < HALF / 32; ++c) tmem_ld_32x32b_x32(tl + TM_S + g * HALF + 32 * c, &qv[32 * c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.dq_free());
-      // warpgroup 0 stages over Q_i, which dK_i (issued after dQ_i) may still be
-      // reading; warpgroup 1 stages over dO_i, last read by dV_i (before dQ_i)
-      if (g == 0 && !warp_wait(bar.dk_done(), ph)) {
-        ok = false;
-        break;
-      }
-      {
+        for (int c = 0; c < NC / 32; ++c) tmem_ld_32x32b_x32(tl + TM_S + col0 + 32 * c, &qv[32 * c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.dq_free());
+        // warpgroup 0 stages over Q_i, which dK_i (issued after dQ_i) may still be
+        // reading; warpgroup 1 stages over dO_i, last read by dV_i (before dQ_i)
+        if (col0 == 0 && !warp_wait(bar.dk_done(), ph)) return false;
         const uint32_t stg = sStage + st * STAGE_BYTES + row * 128;
 #pragma unroll
-        for (int c4 = 0; c4 < HALF / 4; ++c4) {  // 16-byte chunk c4 of this row's HALF values
-          const int col = g * HALF + 4 * c4;      // first d column of the chunk
+        for (int c4 = 0; c4 < NC / 4; ++c4) {  // 16-byte chunk c4 of this row's NC values
+          const int col = col0 + 4 * c4;       // first d column of the chunk
           const uint32_t box = col >> 5, chunk = (col & 31) >> 2;
           st_shared_v4(stg + box * DQ_BOX_BYTES + ((chunk ^ (row & 7)) << 4), qv[4 * c4], qv[4 * c4 + 1],
                        qv[4 * c4 + 2], qv[4 * c4 + 3]);
         }
+        return true;
+      };
+      const bool staged = (g == 0) ? dq_out(std::integral_constant<int, C::DQ_COLS0>{}, 0)
+                                   : dq_out(std::integral_constant<int, C::DQ_COLS1>{}, C::DQ_COLS0);
+      if (!staged) {
+        ok = false;
+        break;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -565,8 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * mul, __uint_as_float(v[q4 * 8 + 2 * e + 1]) * mul);
-          // row-major [128 keys][D] bf16 with 16-byte chunks swizzled by row
-          st_shared_v4(stage_out + row * (2 * D) + ((c16 ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+          // row-major [128 keys][DP] bf16 with 16-byte chunks swizzled by row
+          st_shared_v4(stage_out + row * (2 * C::DP) + ((c16 ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
         }
       }
     }
@@ -579,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = idx / CHUNKS, c16 = idx % CHUNKS;
         if (k0 + rr < N)
           st_global_v4(gout + static_cast<size_t>(rr) * (2 * D) + c16 * 16,
-                       ld_shared_v4(stage_out + rr * (2 * D) + ((c16 ^ (rr & 7)) << 4)));
+                       ld_shared_v4(stage_out + rr * (2 * C::DP) + ((c16 ^ (rr & 7)) << 4)));
       }
     }
   }
@@ -622,7 +642,7 @@ cudaError_t launch_main(const BwdParams& p, const BwdMaps& m, unsigned grid, cud
 }  // namespace
 
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s) {
-  if (p.d != 128 && p.d != 64) return cudaErrorNotSupported;
+  if (p.d != 128 && p.d != 96 && p.d != 64) return cudaErrorNotSupported;
   const long long np = npad128(p.N);
   const long long prep_rows = static_cast<long long>(p.BH) * np;
   const long long prep_blocks = (prep_rows + 7) / 8;
@@ -636,8 +656,9 @@ cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_
       p.dq_acc, p.BH, p.N, p.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = p.d == 128 ? launch_main<128>(p, m, static_cast<unsigned>(grid), s)
-                 : launch_main<64>(p, m, static_cast<unsigned>(grid), s);
+  e = p.d == 128  ? launch_main<128>(p, m, static_cast<unsigned>(grid), s)
+      : p.d == 96 ? launch_main<96>(p, m, static_cast<unsigned>(grid), s)
+                  : launch_main<64>(p, m, static_cast<unsigned>(grid), s);
   if (e != cudaSuccess) return e;
   fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
       p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8, p.scale);

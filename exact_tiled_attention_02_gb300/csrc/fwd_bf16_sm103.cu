@@ -24,7 +24,7 @@
 //              a ten-warp CTA costs as much as twelve; 168 per thread)
 // Tensor memory (512 columns x 128 lanes, 32-bit):
 //   [0,128) S0 (P0 as packed bf16 in its first 64 columns), [128,256) S1 / P1,
-//   [256,256+D) O0, [384,384+D) O1.
+//   [256,256+DP) O0, [384,384+DP) O1 (DP = D rounded up to 64: see Cfg).
 // Shared memory (1024-byte aligned, 128-byte swizzled): Q0, Q1, a ring of
 // STAGES K/V tiles, barriers.
 // The two query tiles ping-pong: while the softmax warps of one tile turn
@@ -59,12 +59,19 @@ constexpr uint32_t kTmemO = 256;  // + 128 * tile
 // 3.7e-4 at 2^8 to 6.1e-4 at 2^64.)
 constexpr float kRescaleThreshold = 8.0f;
 
+// D = 64, 96 or 128.  Tiles in shared memory are DP = D rounded up to a
+// multiple of 64 columns wide (whole 128-byte swizzle atoms); for D = 96 the
+// TMA zero-fills columns 96..127.  Q K^T contracts over the D real columns
+// only.  P V runs with N = DP: a 128-byte-swizzled MN-major V operand is laid
+// out in 64-column atoms, so N = 96 is not one of its layouts, and the zero
+// columns of V only produce zero columns of O, which are never read.
 template <int D>
 struct Cfg {
-  static constexpr int STAGES = (D == 128) ? 2 : 3;
-  static constexpr int BOXES = D / 64;         // 64-column (128-byte) boxes per row
-  static constexpr int Q_BYTES = BR * D * 2;   // one query tile
-  static constexpr int KV_BYTES = BC * D * 2;  // one K or one V tile
+  static constexpr int DP = (D + 63) / 64 * 64;
+  static constexpr int STAGES = (DP == 128) ? 2 : 3;
+  static constexpr int BOXES = DP / 64;         // 64-column (128-byte) boxes per row
+  static constexpr int Q_BYTES = BR * DP * 2;   // one query tile
+  static constexpr int KV_BYTES = BC * DP * 2;  // one K or one V tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
@@ -74,7 +81,7 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(D <= 128, "tensor memory budget");
+  static_assert(D % 32 == 0 && DP <= 128, "tensor memory budget");
 };
 
 template <int STAGES>
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BR, BC, 0, 0);  // Q: K-major, K tile: K-major
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, D, 0, 1);   // P (TMEM), V tile: MN-major
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, C::DP, 0, 1);  // P (TMEM), V tile: MN-major
       auto issue_s = [&](int t, int it) {  // S_t = Q_t K_it^T
         const uint32_t kbase = sK + (it % C::STAGES) * C::KV_BYTES;
         const uint32_t qbase = sQ + t * C::Q_BYTES;
@@ -505,6 +512,7 @@ cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_
   const bool win = p.window_r >= 0;
   if (p.d == 128) return win ? launch_d<128, true>(p, m, s) : launch_d<128, false>(p, m, s);
   if (p.d == 64) return win ? launch_d<64, true>(p, m, s) : launch_d<64, false>(p, m, s);
+  if (p.d == 96) return win ? launch_d<96, true>(p, m, s) : launch_d<96, false>(p, m, s);
   return cudaErrorInvalidValue;
 }
 

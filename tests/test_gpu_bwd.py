@@ -75,6 +75,10 @@ BWD_CASES = [
     (2, 2, 300, 64, 0, 8.0),
     (1, 1, 513, 64, 0, 1.0),
     (1, 2, 700, 64, 65, 1.0),
+    (1, 1, 1, 96, 0, 1.0),
+    (1, 2, 200, 96, 0, 1.0),
+    (1, 1, 513, 96, 0, 8.0),
+    (1, 2, 700, 96, 65, 1.0),
 ]
 
 
@@ -100,13 +104,37 @@ def test_bwd_deterministic_dk_dv():
     assert _rel(_np(a[0]), _np(b[0])) <= 1e-3
 
 
-def test_bwd_d64_large_sampled_heads():
-    """d = 64 at a size with many key and query tiles (B=2, H=8, N=2048)."""
+@pytest.mark.parametrize("d", [64, 96, 128])
+def test_bwd_guard_bands(d):
+    """dQ, dK and dV are written exactly inside [B,H,N,d]: canaries around
+    them stay untouched for a ragged N."""
     dev = _dev()
-    q, k, v, do = inputs.make_inputs(2, 8, 2048, 64, "bf16", seed=64, with_do=True)
-    dq, dk, dv = _run(q, k, v, do, 0.125, 0, dev)
+    fa = _fa()
+    B, H, N = 1, 2, 200
+    q, k, v, do = (t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=21, with_do=True))
+    o, lse = fa.fa_fwd(q, k, v)
+    pad = 4096
+    n = B * H * N * d
+    bufs = [torch.full((2 * pad + n,), 5.0, device=dev, dtype=torch.bfloat16) for _ in range(3)]
+    dq, dk, dv = (b[pad:pad + n].view(B, H, N, d) for b in bufs)
+    fa.fa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for b in bufs:
+        assert torch.all(b[:pad] == 5.0) and torch.all(b[-pad:] == 5.0)
+    refs = oracle.dense_backward(_np(q), _np(k), _np(v), _np(do), 1 / np.sqrt(d))
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        _check_grad(name, _np(g), r, d)
+
+
+@pytest.mark.parametrize("d", [64, 96])
+def test_bwd_large_sampled_heads(d):
+    """d = 64 and 96 at a size with many key and query tiles (B=2, H=8,
+    N=2048), two whole heads against the oracle."""
+    dev = _dev()
+    q, k, v, do = inputs.make_inputs(2, 8, 2048, d, "bf16", seed=d, with_do=True)
+    dq, dk, dv = _run(q, k, v, do, 1 / np.sqrt(d), 0, dev)
     for b, h in ((0, 0), (1, 7)):
-        refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), 0.125)
+        refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), 1 / np.sqrt(d))
         for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
             assert _rel(_np(g), r) <= 1e-2, (name, b, h, _rel(_np(g), r))
 
@@ -138,11 +166,11 @@ def test_workload5_full_size_sampled_heads():
 def test_bwd_unsupported_requests():
     dev = _dev()
     fa = _fa()
-    x = torch.zeros(1, 1, 8, 96, device=dev, dtype=torch.bfloat16)
+    x = torch.zeros(1, 1, 8, 80, device=dev, dtype=torch.bfloat16)
     lse = torch.zeros(1, 1, 8, device=dev, dtype=torch.float32)
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(x, x, x, x, lse, x)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # bf16 head dimensions are 64 and 128
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # bf16 head dimensions are 64, 96 and 128
     y = torch.zeros(1, 1, 8, 132, device=dev, dtype=torch.float32)
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(y, y, y, y, lse, y)

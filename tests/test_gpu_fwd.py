@@ -84,6 +84,10 @@ BF16_CASES = [
     (1, 2, 1000, 64, 257, 1.0),
     (1, 1, 640, 128, 257, 8.0),
     (1, 1, 257, 128, 513, 1.0),
+    (1, 1, 1, 96, 0, 1.0),
+    (1, 2, 129, 96, 0, 1.0),
+    (2, 1, 513, 96, 0, 8.0),
+    (1, 2, 700, 96, 65, 1.0),
 ]
 
 
@@ -109,11 +113,12 @@ def test_bf16_deterministic_and_no_lse():
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
 
 
-def test_bf16_guard_bands():
+@pytest.mark.parametrize("d", [64, 96, 128])
+def test_bf16_guard_bands(d):
     """Outputs are written exactly inside [B,H,N,d] / [B,H,N]: canaries around
     them stay untouched for a ragged N."""
     dev = _dev()
-    B, H, N, d = 1, 3, 200, 128
+    B, H, N = 1, 3, 200
     q, k, v = (t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=9))
     pad = 4096
     obuf = torch.full((2 * pad + B * H * N * d,), 7.0, device=dev, dtype=torch.bfloat16)
@@ -160,6 +165,29 @@ def test_full_size_workloads_sampled(index):
         _check_bf16(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, (index, b, h))
 
 
+@pytest.mark.parametrize("window", [0, 257])
+def test_bf16_d96_large_sampled(window):
+    """d = 96 (tiles padded to 128 columns in shared memory) at B=2, H=8,
+    N=4096: sampled rows of three heads against the oracle, plus the
+    convex-hull property on every output."""
+    dev = _dev()
+    B, H, N, d = 2, 8, 4096, 96
+    q, k, v = inputs.make_inputs(B, H, N, d, "bf16", seed=96 + window)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = _fa().fa_fwd(qd, kd, vd, window=window)
+    torch.cuda.synchronize()
+    assert _fa().fa_last_device_status() == 0
+    vmax = vd.float().amax(dim=2, keepdim=True)
+    vmin = vd.float().amin(dim=2, keepdim=True)
+    assert bool(((o.float() <= vmax + 2e-2) & (o.float() >= vmin - 2e-2)).all())
+    rng = np.random.default_rng(96)
+    for b, h in ((0, 0), (1, 7), (int(rng.integers(B)), int(rng.integers(H)))):
+        rows = _sample_rows(N, rng)
+        o_ref, lse_ref = oracle.dense_forward_rows(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), 1 / np.sqrt(d), rows,
+                                                   window=window)
+        _check_bf16(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, (b, h, window))
+
+
 def test_bounded_wait_times_out_and_context_survives():
     dev = _dev()
     fa = _fa()
@@ -186,7 +214,7 @@ def test_binding_rejects_bad_tensors():
         fa.fa_fwd(q, q, q.transpose(2, 3).contiguous().transpose(2, 3))
     with pytest.raises(fa.FaError):
         fa.fa_fwd(q, q, q, window=4)
-    x = torch.zeros(1, 1, 8, 96, device=dev, dtype=torch.bfloat16)
+    x = torch.zeros(1, 1, 8, 80, device=dev, dtype=torch.bfloat16)
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd(x, x, x)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
