@@ -125,7 +125,7 @@ def fa_fwd(q, k, v, scale: float | None = None, window: int = 0, o=None, lse=Non
            stream=None):
     """O = softmax(Q K^T * scale) V on the GPU; returns ``(o, lse)``.
 
-    ``q, k, v``: contiguous [B, H, N, d] bf16 (d in {64, 96, 128}) or float32
+    ``q, k, v``: contiguous [B, H, N, d] bf16 (d in {64, 96, 128, 256}) or float32
     (d <= 128) CUDA tensors.  ``scale`` defaults to 1/sqrt(d).  ``window``:
     0 = unmasked, else the odd full width of the local window.  ``o``/``lse``
     may be given to write into existing buffers; ``lse`` is float32 [B, H, N]

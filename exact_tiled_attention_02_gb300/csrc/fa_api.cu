@@ -110,7 +110,7 @@ fa_status check_common(int B, int H, int N, int d, float scale, int window, fa_d
   const long long bh = static_cast<long long>(B) * H;
   if (bh > 0x7fffffffLL) return FA_ERR_INVALID;
   if (bh * N > (1LL << 40) / (d > 0 ? d : 1)) return FA_ERR_INVALID;
-  if (dt == FA_DTYPE_BF16 && d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dt == FA_DTYPE_BF16 && d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (dt == FA_DTYPE_F32 && d > 128) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -220,6 +220,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   const fa_status c = check_common(B, H, N, d, scale, window, dt);
   if (c != FA_OK) return c;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
+  if (dt == FA_DTYPE_BF16 && d == 256) return FA_ERR_UNSUPPORTED;  // forward only at d = 256
 
   BwdParams p{};
   p.q = q;

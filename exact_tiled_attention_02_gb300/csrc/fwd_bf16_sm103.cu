@@ -513,6 +513,7 @@ cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_
   if (p.d == 128) return win ? launch_d<128, true>(p, m, s) : launch_d<128, false>(p, m, s);
   if (p.d == 64) return win ? launch_d<64, true>(p, m, s) : launch_d<64, false>(p, m, s);
   if (p.d == 96) return win ? launch_d<96, true>(p, m, s) : launch_d<96, false>(p, m, s);
+  if (p.d == 256) return launch_fwd_bf16_d256(p, m, s);
   return cudaErrorInvalidValue;
 }
 

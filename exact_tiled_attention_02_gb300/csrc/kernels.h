@@ -63,6 +63,7 @@ struct BwdMaps {
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
+cudaError_t launch_fwd_bf16_d256(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
 cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
 // Byte size of the backward workspace and the offsets of its lse2 / dsum

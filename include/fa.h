@@ -25,7 +25,8 @@
  *            Every base pointer must be 16-byte aligned.
  * dtype      FA_DTYPE_BF16: Q/K/V/O/dO/dQ/dK/dV are bfloat16, arithmetic is
  *            fp32-accumulated tensor-core math with P rounded to bf16 before
- *            the P V product; d must be 64, 96 or 128.
+ *            the P V product; d must be 64, 96, 128 or 256 (256: forward
+ *            only).
  *            FA_DTYPE_F32: all arrays are float32 and all arithmetic is exact
  *            fp32 on CUDA cores with the accurate expf/logf; 1 <= d <= 128.
  * scale      finite and > 0; usually 1/sqrt(d).
@@ -101,7 +102,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                    owned by the caller, 256-byte aligned; its contents on
  *                    entry do not matter and are undefined on return.
  *   workspace_bytes  its size; smaller than required -> FA_ERR_INVALID.
- * bf16 with d = 64, 96 or 128 (other d return FA_ERR_UNSUPPORTED), or float32
+ * bf16 with d = 64, 96 or 128 (other d, 256 included, return
+ * FA_ERR_UNSUPPORTED), or float32
  * with 1 <= d <= 128 (CUDA cores; one warp per query row for dQ and one per
  * key row for dK and dV, so dK and dV need no atomics and the float32 path
  * is bitwise repeatable).

@@ -79,7 +79,7 @@ def bwd(b, ws=P, ws_bytes=1 << 30, dt=1, d=128, N=8, window=0, lse=P, scale=0.1)
     (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1), (dict(d=0), 1),
     (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(window=4), 1), (dict(window=256), 1), (dict(dt=7), 1),
-    (dict(d=80), 2), (dict(d=32), 2), (dict(d=256), 2), (dict(dt=0, d=129), 2),
+    (dict(d=80), 2), (dict(d=32), 2), (dict(d=192), 2), (dict(d=512), 2), (dict(dt=0, d=129), 2),
 ])
 def test_fwd_rejects_on_host(b, kw, code):
     assert fwd(b, **kw) == code
@@ -87,7 +87,7 @@ def test_fwd_rejects_on_host(b, kw, code):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=0), 1), (dict(ws=P + 16), 1), (dict(ws_bytes=100), 1), (dict(lse=0), 1),
-    (dict(window=2), 1), (dict(scale=0.0), 1), (dict(d=80), 2), (dict(d=32), 2), (dict(dt=0, d=129), 2),
+    (dict(window=2), 1), (dict(scale=0.0), 1), (dict(d=80), 2), (dict(d=256), 2), (dict(d=32), 2), (dict(dt=0, d=129), 2),
 ])
 def test_bwd_rejects_on_host(b, kw, code):
     assert bwd(b, **kw) == code

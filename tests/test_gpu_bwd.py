@@ -171,6 +171,10 @@ def test_bwd_unsupported_requests():
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(x, x, x, x, lse, x)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED  # bf16 head dimensions are 64, 96 and 128
+    z = torch.zeros(1, 1, 8, 256, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(z, z, z, z, lse, z)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # d = 256 has a forward only
     y = torch.zeros(1, 1, 8, 132, device=dev, dtype=torch.float32)
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(y, y, y, y, lse, y)

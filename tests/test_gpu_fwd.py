@@ -88,6 +88,12 @@ BF16_CASES = [
     (1, 2, 129, 96, 0, 1.0),
     (2, 1, 513, 96, 0, 8.0),
     (1, 2, 700, 96, 65, 1.0),
+    (1, 1, 1, 256, 0, 1.0),
+    (1, 2, 129, 256, 0, 1.0),
+    (2, 1, 513, 256, 0, 8.0),
+    (1, 1, 300, 256, 3, 1.0),
+    (1, 2, 700, 256, 65, 1.0),
+    (1, 1, 640, 256, 257, 8.0),
 ]
 
 
@@ -113,7 +119,7 @@ def test_bf16_deterministic_and_no_lse():
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
 
 
-@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
 def test_bf16_guard_bands(d):
     """Outputs are written exactly inside [B,H,N,d] / [B,H,N]: canaries around
     them stay untouched for a ragged N."""
@@ -165,14 +171,15 @@ def test_full_size_workloads_sampled(index):
         _check_bf16(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, (index, b, h))
 
 
-@pytest.mark.parametrize("window", [0, 257])
-def test_bf16_d96_large_sampled(window):
-    """d = 96 (tiles padded to 128 columns in shared memory) at B=2, H=8,
+@pytest.mark.parametrize("d,window", [(96, 0), (96, 257), (256, 0), (256, 257)])
+def test_bf16_other_d_large_sampled(d, window):
+    """d = 96 (tiles padded to 128 columns in shared memory) and d = 256 (one
+    query tile per CTA, K/V streamed in half-width chunks) at B=2, H=8,
     N=4096: sampled rows of three heads against the oracle, plus the
     convex-hull property on every output."""
     dev = _dev()
-    B, H, N, d = 2, 8, 4096, 96
-    q, k, v = inputs.make_inputs(B, H, N, d, "bf16", seed=96 + window)
+    B, H, N = 2, 8, 4096
+    q, k, v = inputs.make_inputs(B, H, N, d, "bf16", seed=d + window)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     o, lse = _fa().fa_fwd(qd, kd, vd, window=window)
     torch.cuda.synchronize()
@@ -180,7 +187,7 @@ def test_bf16_d96_large_sampled(window):
     vmax = vd.float().amax(dim=2, keepdim=True)
     vmin = vd.float().amin(dim=2, keepdim=True)
     assert bool(((o.float() <= vmax + 2e-2) & (o.float() >= vmin - 2e-2)).all())
-    rng = np.random.default_rng(96)
+    rng = np.random.default_rng(d)
     for b, h in ((0, 0), (1, 7), (int(rng.integers(B)), int(rng.integers(H)))):
         rows = _sample_rows(N, rng)
         o_ref, lse_ref = oracle.dense_forward_rows(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), 1 / np.sqrt(d), rows,
