@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < nsteps; ++it) {
         // tile it's dQ is staged in stage it % STAGES: warpgroup 0's columns over
         // the Q half, warpgroup 1's over the dO half.  Reduce the Q half first
-        // and reload Q (which the next tile's first product needs) as soon as
+        // and reload Q (which the first product of a step needs) as soon as
         // that half has been read, then the dO half.
         const int st = it % STAGES;
         const uint32_t sbase = sStage + st * STAGE_BYTES;
@@ -332,15 +332,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < C::QBOXES; ++b)
           tma_reduce_add_3d(&tmdq, sbase + b * DQ_BOX_BYTES, 32 * b, q0, bh);
         bulk_commit_group();
+        // Q_{it+STAGES} is loaded before the dO half's reduction is issued, so
+        // the load does not queue behind that reduction's read of shared memory
+        if (loaded < nsteps) {
+          bulk_wait_read_all();  // the Q half has been read
+          load_q(loaded);
+        }
         if (!mbar_wait_backoff(bar.staged_o(st), (it / STAGES) & 1, wc)) break;
 #pragma unroll
         for (int b = C::QBOXES; b < C::DQ_BOXES; ++b)
           tma_reduce_add_3d(&tmdq, sbase + b * DQ_BOX_BYTES, 32 * b, q0, bh);
         bulk_commit_group();
         if (loaded < nsteps) {
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the Q half has been read
-          load_q(loaded);
-          bulk_wait_read_all();
+          bulk_wait_read_all();  // the dO half has been read
           load_o(loaded);
           ++loaded;
         }
