@@ -332,8 +332,8 @@ def main():
         kernels["bwd"] = {"ms": bwd_ms, "tflops": flops_bwd / (bwd_ms * 1e-3) / 1e12}
         kernels["bwd"]["frac"] = kernels["bwd"]["tflops"] / peak
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    src_file = {"fwd": "fwd_bf16_sm103.cu", "bwd": "bwd_bf16_sm103.cu"}[dom]
-    traffic = ncu_traffic(f"{dom}_bf16_sm103_{w.name}.md", src_file)
+    kname = {"fwd": "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103", "bwd": "bwd_bf16_sm103"}[dom]
+    traffic = ncu_traffic(f"{kname}_{w.name}.md", kname + ".cu")
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(kernels[dom]["tflops"], 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
                 "traffic": traffic, "peak_source": f"{peak_src} bf16 dense (burst)"}
