@@ -49,6 +49,9 @@ def parse_args():
                     help="B,H,N,d[,window[,qk_mult]]: a bf16 problem of another shape instead of a workload "
                          "(for measuring other head dimensions; not a bench line of record)")
     ap.add_argument("--no-bwd", action="store_true", help="forward only")
+    ap.add_argument("--schedule", choices=["query-major", "key-major"], default="query-major",
+                    help="forward loop order; key-major (outer loop over key tiles, O in device memory between "
+                         "steps) is a comparison schedule and runs forward only")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -259,9 +262,16 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    with_bwd = not args.no_bwd
+    key_major = args.schedule == "key-major"
+    with_bwd = not args.no_bwd and not key_major
     q, k, v, do = inputs.workload_inputs(w, with_do=True)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    fwd_fn = fa.fa_fwd
+    if key_major:
+        km_ws = torch.empty(fa.fa_fwd_key_major_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+
+        def fwd_fn(q_, k_, v_, **kw):
+            return fa.fa_fwd_key_major(q_, k_, v_, workspace=km_ws, **kw)
     od = torch.empty_like(qd)
     lsed = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
     dqd, dkd, dvd = (torch.empty_like(qd) for _ in range(3))
@@ -283,7 +293,7 @@ def main():
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        fa.fa_fwd(qd, kd, vd, scale=w.scale, window=w.window, o=od, lse=lsed)
+        fwd_fn(qd, kd, vd, scale=w.scale, window=w.window, o=od, lse=lsed)
         if evs is not None:
             evs[1].record(stream)
         if with_bwd:
@@ -332,7 +342,8 @@ def main():
         kernels["bwd"] = {"ms": bwd_ms, "tflops": flops_bwd / (bwd_ms * 1e-3) / 1e12}
         kernels["bwd"]["frac"] = kernels["bwd"]["tflops"] / peak
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    kname = {"fwd": "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103", "bwd": "bwd_bf16_sm103"}[dom]
+    kname = {"fwd": "fwd_keymajor_sm103" if key_major else "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103",
+             "bwd": "bwd_bf16_sm103"}[dom]
     traffic = ncu_traffic(f"{kname}_{w.name}.md", kname + ".cu")
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(kernels[dom]["tflops"], 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
@@ -340,7 +351,7 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(fa, w, q, k, v, do, with_bwd, dev, min(K, 10), pg)
+        e2e = run_e2e(fa, w, q, k, v, do, with_bwd, dev, min(K, 10), pg, fwd_fn)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -357,6 +368,7 @@ def main():
             "vs_baseline": None, "dtype": w.dtype, "data": data_desc(w),
             "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
                        "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult,
+                       "schedule": args.schedule,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
                        "l2": l2_note(w, qd)},
@@ -364,7 +376,7 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": K * (1 + (3 if with_bwd else 0)),
+            "gpu_launches": K * ((-(-w.N // 128) + 1) if key_major else (1 + (3 if with_bwd else 0))),
             "clocks": clocks,
         }
         print(json.dumps(line))
@@ -373,7 +385,7 @@ def main():
     return 0
 
 
-def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg):
+def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg, fwd_fn=None):
     """Same metric through the public API with pinned host buffers: each step
     copies the step's inputs host->device, runs the pass(es) and copies the
     results back, all inside the timed region."""
@@ -394,7 +406,7 @@ def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg):
         dq_.copy_(hq, non_blocking=True)
         dk_.copy_(hk, non_blocking=True)
         dv_.copy_(hv, non_blocking=True)
-        fa.fa_fwd(dq_, dk_, dv_, scale=w.scale, window=w.window, o=od, lse=ld)
+        (fwd_fn or fa.fa_fwd)(dq_, dk_, dv_, scale=w.scale, window=w.window, o=od, lse=ld)
         if with_bwd:
             ddo.copy_(hdo, non_blocking=True)
             fa.fa_bwd(dq_, dk_, dv_, od, ld, ddo, scale=w.scale, window=w.window, dq=gd[0], dk=gd[1], dv=gd[2],

@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(_HERE, "libfa.so")
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_static_workspace", "fa_last_device_status",
-           "fa_set_wait_limit_us", "fa_selftest_wait_timeout", "fa_status_string", "fa_version")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_static_workspace", "fa_fwd_key_major",
+           "fa_fwd_key_major_workspace_bytes", "fa_last_device_status", "fa_set_wait_limit_us",
+           "fa_selftest_wait_timeout", "fa_status_string", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -43,6 +44,10 @@ def _load() -> ctypes.CDLL:
     L.fa_bwd_static_workspace.restype = i
     L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_bwd_workspace_bytes.restype = sz
+    L.fa_fwd_key_major.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+    L.fa_fwd_key_major.restype = i
+    L.fa_fwd_key_major_workspace_bytes.argtypes = [i, i, i, i]
+    L.fa_fwd_key_major_workspace_bytes.restype = sz
     L.fa_last_device_status.argtypes = [vp]
     L.fa_last_device_status.restype = i
     L.fa_set_wait_limit_us.argtypes = [ctypes.c_longlong]
@@ -113,6 +118,10 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return lib.fa_bwd_workspace_bytes(B, H, N, d)
 
 
+def fa_fwd_key_major_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return lib.fa_fwd_key_major_workspace_bytes(B, H, N, d)
+
+
 def fa_last_device_status(stream=None) -> int:
     return lib.fa_last_device_status(_stream_ptr(stream))
 
@@ -148,6 +157,36 @@ def fa_fwd(q, k, v, scale: float | None = None, window: int = 0, o=None, lse=Non
                     _dtype_code(q), _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_key_major(q, k, v, scale: float | None = None, window: int = 0, o=None, lse=None, want_lse: bool = True,
+                     workspace=None, stream=None):
+    """The forward pass in the key-major loop order (a comparison schedule,
+    bf16 with d = 64 or 128); same results as ``fa_fwd``.  The fp32 workspace
+    for the running statistics is taken from ``workspace`` (a CUDA uint8
+    tensor of at least ``fa_fwd_key_major_workspace_bytes`` bytes) or
+    allocated here with torch."""
+    torch = _torch()
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_qkv(q, o)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if workspace is None:
+        workspace = torch.empty(fa_fwd_key_major_workspace_bytes(B, H, N, d), device=q.device, dtype=torch.uint8)
+    st = lib.fa_fwd_key_major(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(window),
+                              _dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_key_major")
     return o, lse
 
 

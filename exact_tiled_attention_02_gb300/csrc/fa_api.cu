@@ -209,6 +209,47 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return launch_fwd_bf16_tc(p, m, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+size_t fa_fwd_key_major_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL) return 0;
+  return keymajor_workspace_layout(static_cast<int>(bh), N, d, nullptr, nullptr);
+}
+
+fa_status fa_fwd_key_major(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                           int d, float scale, int window, fa_dtype dt, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!q || !k || !v || !o || !workspace) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID;
+  const fa_status c = check_common(B, H, N, d, scale, window, dt);
+  if (c != FA_OK) return c;
+  if (dt != FA_DTYPE_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < fa_fwd_key_major_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
+
+  FwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.BH = B * H;
+  p.N = N;
+  p.d = d;
+  p.window_r = radius(window);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_ns = wait_ns();
+  if (status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+  FwdMaps m;
+  if (!make_map_bf16(&m.q, q, p.BH, N, d, 128) || !make_map_bf16(&m.k, k, p.BH, N, d, 128) ||
+      !make_map_bf16(&m.v, v, p.BH, N, d, 128))
+    return FA_ERR_CUDA;
+  return launch_fwd_keymajor(p, m, workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                  : FA_ERR_CUDA;
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int window, fa_dtype dt,
                  void* workspace, size_t workspace_bytes, void* stream) {

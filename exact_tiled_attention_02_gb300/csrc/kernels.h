@@ -64,6 +64,11 @@ struct BwdMaps {
 cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d256(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
+// Key-major forward (comparison schedule): one launch per key tile, then a
+// finishing launch; workspace = fp32 O~ [BH,N,d], then m and l [BH,N], each
+// section 256-byte aligned.
+cudaError_t launch_fwd_keymajor(const FwdParams& p, const FwdMaps& m, void* workspace, cudaStream_t s);
+size_t keymajor_workspace_layout(int BH, int N, int d, size_t* off_m, size_t* off_l);
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
 cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
 // Byte size of the backward workspace and the offsets of its lse2 / dsum

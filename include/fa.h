@@ -90,6 +90,28 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * The same forward pass as fa_fwd, evaluated in the key-major loop order that
+ * "Compute attention one tile at a time" (TensorViz), fidelity note,
+ * attributes to the original Algorithm 1: the outer loop runs over 128-key
+ * tiles (one launch each, in order on `stream`), and each launch merges that
+ * tile into every query tile's running statistics (the notes' "Derivation:
+ * Incremental Softmax", Steps 2-3), which live in `workspace` between
+ * launches: fp32 unnormalised O~ [B,H,N,d], then m and l [B,H,N], each
+ * section 256-byte aligned; a last launch writes O = O~ / l and lse.  It is
+ * kept as a measured comparison point: every step reads and writes O~ in
+ * device memory, which fa_fwd keeps on chip.
+ *   workspace        at least fa_fwd_key_major_workspace_bytes() bytes,
+ *                    256-byte aligned, owned by the caller; contents on entry
+ *                    do not matter and are undefined on return.
+ * bf16 with d = 64 or 128 only (others return FA_ERR_UNSUPPORTED); other
+ * arguments, results and errors as fa_fwd.
+ */
+fa_status fa_fwd_key_major(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int window, fa_dtype dt,
+                           void* workspace, size_t workspace_bytes, void* stream);
+size_t fa_fwd_key_major_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * Backward pass by recomputation: given Q, K, V, the forward output O, its
  * lse and the output gradient dO, writes dQ, dK, dV (same dtype and layout
  * as Q).  S and P are rebuilt on chip from Q, K and lse; nothing of size

@@ -93,6 +93,26 @@ def test_bwd_rejects_on_host(b, kw, code):
     assert bwd(b, **kw) == code
 
 
+def km(b, ws=P, ws_bytes=1 << 30, dt=1, d=128, N=8, window=0, scale=0.1, o=P):
+    vp = ctypes.c_void_p
+    return b.lib.fa_fwd_key_major(vp(P), vp(P), vp(P), vp(o), vp(0), 1, 1, N, d, scale, window, dt, vp(ws), ws_bytes,
+                                  vp(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), 1), (dict(ws=P + 16), 1), (dict(ws_bytes=100), 1), (dict(o=0), 1), (dict(o=P + 4), 1),
+    (dict(window=2), 1), (dict(scale=0.0), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(dt=0, d=64), 2),
+])
+def test_key_major_rejects_on_host(b, kw, code):
+    assert km(b, **kw) == code
+
+
+def test_key_major_workspace_size(b):
+    assert b.fa_fwd_key_major_workspace_bytes(1, 0, 1, 1) == 0
+    # O~ (2 * 129 rows x 128 fp32), then m and l (258 floats -> 1280 B each)
+    assert b.fa_fwd_key_major_workspace_bytes(2, 1, 129, 128) == 2 * 129 * 128 * 4 + 2 * 1280
+
+
 def test_selftest_rejects_bad_limit(b):
     assert b.lib.fa_selftest_wait_timeout(0, ctypes.c_void_p(0)) == 1
     assert b.lib.fa_selftest_wait_timeout(100001, ctypes.c_void_p(0)) == 1
