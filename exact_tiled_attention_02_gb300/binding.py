@@ -20,8 +20,9 @@ FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5
 FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_static_workspace", "fa_fwd_key_major",
-           "fa_fwd_key_major_workspace_bytes", "fa_last_device_status", "fa_set_wait_limit_us",
-           "fa_selftest_wait_timeout", "fa_status_string", "fa_version")
+           "fa_fwd_key_major_workspace_bytes", "fa_fwd_f32_3xtf32", "fa_fwd_f32_3xtf32_workspace_bytes",
+           "fa_last_device_status", "fa_set_wait_limit_us", "fa_selftest_wait_timeout", "fa_status_string",
+           "fa_version")
 
 
 class FaError(RuntimeError):
@@ -48,6 +49,10 @@ def _load() -> ctypes.CDLL:
     L.fa_fwd_key_major.restype = i
     L.fa_fwd_key_major_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_fwd_key_major_workspace_bytes.restype = sz
+    L.fa_fwd_f32_3xtf32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    L.fa_fwd_f32_3xtf32.restype = i
+    L.fa_fwd_f32_3xtf32_workspace_bytes.argtypes = [i, i, i, i]
+    L.fa_fwd_f32_3xtf32_workspace_bytes.restype = sz
     L.fa_last_device_status.argtypes = [vp]
     L.fa_last_device_status.restype = i
     L.fa_set_wait_limit_us.argtypes = [ctypes.c_longlong]
@@ -122,6 +127,10 @@ def fa_fwd_key_major_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return lib.fa_fwd_key_major_workspace_bytes(B, H, N, d)
 
 
+def fa_fwd_f32_3xtf32_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return lib.fa_fwd_f32_3xtf32_workspace_bytes(B, H, N, d)
+
+
 def fa_last_device_status(stream=None) -> int:
     return lib.fa_last_device_status(_stream_ptr(stream))
 
@@ -187,6 +196,37 @@ def fa_fwd_key_major(q, k, v, scale: float | None = None, window: int = 0, o=Non
                               _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_key_major")
+    return o, lse
+
+
+def fa_fwd_f32_3xtf32(q, k, v, scale: float | None = None, window: int = 0, o=None, lse=None, want_lse: bool = True,
+                      workspace=None, stream=None):
+    """float32 forward on the tensor cores by the 3xTF32 split (d <= 64);
+    same operation and outputs as ``fa_fwd`` on float32 tensors.  The
+    workspace (split copies of Q, K, V) is taken from ``workspace`` (a CUDA
+    uint8 tensor of at least ``fa_fwd_f32_3xtf32_workspace_bytes`` bytes) or
+    allocated here with torch."""
+    torch = _torch()
+    _check_qkv(q, k, v)
+    if q.dtype != torch.float32:
+        raise TypeError("fa_fwd_f32_3xtf32 takes float32 tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _check_qkv(q, o)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if workspace is None:
+        workspace = torch.empty(fa_fwd_f32_3xtf32_workspace_bytes(B, H, N, d), device=q.device, dtype=torch.uint8)
+    st = lib.fa_fwd_f32_3xtf32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(window),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_f32_3xtf32")
     return o, lse
 
 

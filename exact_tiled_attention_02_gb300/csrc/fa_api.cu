@@ -49,9 +49,7 @@ cudaError_t status_ptr(unsigned int** out) {
   return st.err;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef EncodeTiledFnPtr EncodeTiledFn;
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point, so the
 // library does not link against libcuda directly.
@@ -248,6 +246,45 @@ fa_status fa_fwd_key_major(const void* q, const void* k, const void* v, void* o,
     return FA_ERR_CUDA;
   return launch_fwd_keymajor(p, m, workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
                                                                                                   : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_f32_3xtf32_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL) return 0;
+  return f32_tc_workspace_layout(static_cast<int>(bh), N, nullptr);
+}
+
+fa_status fa_fwd_f32_3xtf32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
+                            int N, int d, float scale, int window, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!q || !k || !v || !o || !workspace) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID;
+  const fa_status c = check_common(B, H, N, d, scale, window, FA_DTYPE_F32);
+  if (c != FA_OK) return c;
+  if (d > 64) return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < fa_fwd_f32_3xtf32_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
+
+  FwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.BH = B * H;
+  p.N = N;
+  p.d = d;
+  p.window_r = radius(window);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_ns = wait_ns();
+  if (status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return FA_ERR_CUDA;
+  return launch_fwd_f32_tc(p, workspace, fn, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                : FA_ERR_CUDA;
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,

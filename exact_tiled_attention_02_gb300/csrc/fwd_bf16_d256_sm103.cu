@@ -52,8 +52,8 @@ constexpr int NCHUNK = 5;                      // ring depth
 constexpr int OFF_Q = 0;
 constexpr int OFF_RING = OFF_Q + Q_BYTES;
 constexpr int OFF_BAR = OFF_RING + NCHUNK * CHUNK_BYTES;
-// q_full, full[NCHUNK], empty[NCHUNK], s_full[2], p_full, o_done, drain
-constexpr int NBAR = 1 + 2 * NCHUNK + 5;
+// q_full, full[NCHUNK], empty[NCHUNK], s_full[2], p_full[2], o_done, drain
+constexpr int NBAR = 1 + 2 * NCHUNK + 6;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
@@ -67,9 +67,12 @@ struct Bars {
   __device__ uint32_t full(int c) const { return base + 8 * (1 + c); }
   __device__ uint32_t empty(int c) const { return base + 8 * (1 + NCHUNK + c); }
   __device__ uint32_t s_full(int b) const { return base + 8 * (1 + 2 * NCHUNK + b); }
-  __device__ uint32_t p_full() const { return base + 8 * (3 + 2 * NCHUNK); }
-  __device__ uint32_t o_done() const { return base + 8 * (4 + 2 * NCHUNK); }
-  __device__ uint32_t drain() const { return base + 8 * (5 + 2 * NCHUNK); }
+  // P_j of buffer b = j % 2 is in tensor memory.  One barrier per buffer: the
+  // softmax may finish P_{j+1} before the MMA warp has waited for P_j, but it
+  // cannot finish P_{j+2} (that needs S_{j+2}, issued after P_j V_j)
+  __device__ uint32_t p_full(int b) const { return base + 8 * (3 + 2 * NCHUNK + b); }
+  __device__ uint32_t o_done() const { return base + 8 * (5 + 2 * NCHUNK); }
+  __device__ uint32_t drain() const { return base + 8 * (6 + 2 * NCHUNK); }
 };
 
 template <bool WIN>
@@ -114,7 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar.s_full(0), 1);
     mbar_init(bar.s_full(1), 1);
-    mbar_init(bar.p_full(), 4);  // one arrive per softmax warp
+    mbar_init(bar.p_full(0), 4);  // one arrive per softmax warp
+    mbar_init(bar.p_full(1), 4);
     mbar_init(bar.o_done(), 1);
     mbar_init(bar.drain(), 1);
     *abort_flag = 0;
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_pv = [&](int j) -> bool {  // O (+)= P_j V_j, one V chunk per half of O
-        if (!mbar_wait(bar.p_full(), j & 1, wc)) return false;
+        if (!mbar_wait(bar.p_full(j & 1), (j >> 1) & 1, wc)) return false;
         tc_fence_after();
         const uint32_t a_tm = tmem + 128 * (j & 1);
         for (int half = 0; half < 2; ++half, ++seq) {
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full());
+      if (lane == 0) mbar_arrive(bar.p_full(j & 1));
       l = l * alpha + rsum;
     }
 

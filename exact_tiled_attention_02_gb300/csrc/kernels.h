@@ -64,6 +64,16 @@ struct BwdMaps {
 cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d256(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
+// cuTensorMapEncodeTiled's signature (resolved at run time by the C-ABI layer)
+typedef CUresult (*EncodeTiledFnPtr)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// fp32 forward on the tensor cores by the 3xTF32 split (d <= 64): workspace =
+// Q hi, Q lo, K hi, K lo as [BH][N][64] fp32, then V^T hi, V^T lo as
+// [BH][64][Npad] fp32 (Npad = N rounded up to 64), each 256-byte aligned;
+// off (may be null) receives the six section offsets.
+size_t f32_tc_workspace_layout(int BH, int N, size_t off[6]);
+cudaError_t launch_fwd_f32_tc(const FwdParams& p, void* workspace, EncodeTiledFnPtr encode, cudaStream_t s);
 // Key-major forward (comparison schedule): one launch per key tile, then a
 // finishing launch; workspace = fp32 O~ [BH,N,d], then m and l [BH,N], each
 // section 256-byte aligned.

@@ -113,6 +113,29 @@ def test_key_major_workspace_size(b):
     assert b.fa_fwd_key_major_workspace_bytes(2, 1, 129, 128) == 2 * 129 * 128 * 4 + 2 * 1280
 
 
+def tf(b, ws=P, ws_bytes=1 << 30, d=64, N=8, window=0, scale=0.1, o=P, lse=0):
+    vp = ctypes.c_void_p
+    return b.lib.fa_fwd_f32_3xtf32(vp(P), vp(P), vp(P), vp(o), vp(lse), 1, 1, N, d, scale, window, vp(ws), ws_bytes,
+                                   vp(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), 1), (dict(ws=P + 16), 1), (dict(ws_bytes=100), 1), (dict(o=0), 1), (dict(o=P + 4), 1),
+    (dict(lse=P + 2), 1), (dict(window=2), 1), (dict(scale=0.0), 1), (dict(N=0), 1), (dict(d=65), 2),
+    (dict(d=128), 2),
+])
+def test_3xtf32_rejects_on_host(b, kw, code):
+    assert tf(b, **kw) == code
+
+
+def test_3xtf32_workspace_size(b):
+    assert b.fa_fwd_f32_3xtf32_workspace_bytes(1, 1, 0, 8) == 0
+    # Q, K hi/lo: 4 x (2*100 rows x 64 fp32); V^T hi/lo: 2 x (2 x 64 x 128 fp32), each rounded to 256 B
+    rows = (2 * 100 * 64 * 4 + 255) // 256 * 256
+    vt = 2 * 64 * 128 * 4
+    assert b.fa_fwd_f32_3xtf32_workspace_bytes(2, 1, 100, 16) == 4 * rows + 2 * vt
+
+
 def test_selftest_rejects_bad_limit(b):
     assert b.lib.fa_selftest_wait_timeout(0, ctypes.c_void_p(0)) == 1
     assert b.lib.fa_selftest_wait_timeout(100001, ctypes.c_void_p(0)) == 1
