@@ -49,6 +49,10 @@ def parse_args():
                     help="B,H,N,d[,window[,qk_mult]]: a bf16 problem of another shape instead of a workload "
                          "(for measuring other head dimensions; not a bench line of record)")
     ap.add_argument("--no-bwd", action="store_true", help="forward only")
+    ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16", help="dtype of a --shape problem")
+    ap.add_argument("--f32-path", choices=["simt", "3xtf32"], default="simt",
+                    help="float32 forward: exact CUDA-core kernel, or the tensor-core 3xTF32 split (d <= 64, "
+                         "forward only)")
     ap.add_argument("--schedule", choices=["query-major", "key-major"], default="query-major",
                     help="forward loop order; key-major (outer loop over key tiles, O in device memory between "
                          "steps) is a comparison schedule and runs forward only")
@@ -244,7 +248,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    w = configs.WORKLOADS[args.workload] if args.shape is None else configs.custom_workload(args.shape)
+    w = configs.WORKLOADS[args.workload] if args.shape is None else configs.custom_workload(args.shape, args.dtype)
 
     if args.impl == "reference":
         if rank != 0:
@@ -263,7 +267,8 @@ def main():
         pg = dist
 
     key_major = args.schedule == "key-major"
-    with_bwd = not args.no_bwd and not key_major
+    tf32x3 = w.dtype == "f32" and args.f32_path == "3xtf32"
+    with_bwd = not args.no_bwd and not key_major and not tf32x3
     q, k, v, do = inputs.workload_inputs(w, with_do=True)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     fwd_fn = fa.fa_fwd
@@ -272,6 +277,11 @@ def main():
 
         def fwd_fn(q_, k_, v_, **kw):
             return fa.fa_fwd_key_major(q_, k_, v_, workspace=km_ws, **kw)
+    if tf32x3:
+        tc_ws = torch.empty(fa.fa_fwd_f32_3xtf32_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+
+        def fwd_fn(q_, k_, v_, **kw):
+            return fa.fa_fwd_f32_3xtf32(q_, k_, v_, workspace=tc_ws, **kw)
     od = torch.empty_like(qd)
     lsed = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
     dqd, dkd, dvd = (torch.empty_like(qd) for _ in range(3))
@@ -335,19 +345,29 @@ def main():
     value = weak_scaling_value(flops_step, world, ms_per_step)
 
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops"]
+    peak, bound, peak_note = peaks["bf16_tflops"], "tensor", f"{peak_src} bf16 dense (burst)"
+    if tf32x3:
+        # three tf32 products per float32 product; tf32 at the nominal tf32/bf16 ratio of the measured bf16 peak
+        peak = peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0
+        peak_note = f"{peak_src} bf16 dense (burst) x 1.1/2.25 (nominal tf32/bf16) / 3 (3xTF32 products)"
+    elif w.dtype == "f32":
+        # CUDA-core fp32 FMA: SMs x 128 lanes x 2 flops x 2.07 GHz (the maximum SM clock)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak, bound = sms * 128 * 2 * 2.07e9 / 1e12, "alu"
+        peak_note = f"fp32 FMA: {sms} SMs x 128 lanes x 2 flops x 2.07 GHz"
     kernels = {"fwd": {"ms": fwd_ms, "tflops": flops_fwd / (fwd_ms * 1e-3) / 1e12}}
     kernels["fwd"]["frac"] = kernels["fwd"]["tflops"] / peak
     if with_bwd:
         kernels["bwd"] = {"ms": bwd_ms, "tflops": flops_bwd / (bwd_ms * 1e-3) / 1e12}
         kernels["bwd"]["frac"] = kernels["bwd"]["tflops"] / peak
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    kname = {"fwd": "fwd_keymajor_sm103" if key_major else "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103",
-             "bwd": "bwd_bf16_sm103"}[dom]
+    kname = {"fwd": "fwd_keymajor_sm103" if key_major else "fwd_f32_tc_sm103" if tf32x3 else
+             "fwd_f32_simt" if w.dtype == "f32" else "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103",
+             "bwd": "bwd_f32_simt" if w.dtype == "f32" else "bwd_bf16_sm103"}[dom]
     traffic = ncu_traffic(f"{kname}_{w.name}.md", kname + ".cu")
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(kernels[dom]["tflops"], 2),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
-                "traffic": traffic, "peak_source": f"{peak_src} bf16 dense (burst)"}
+    roofline = {"bound": bound, "kernel": dom, "achieved": round(kernels[dom]["tflops"], 2),
+                "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
+                "traffic": traffic, "peak_source": peak_note}
 
     e2e = None
     if not args.no_e2e:
@@ -369,6 +389,7 @@ def main():
             "config": {"workload": w.name + (" + bwd on the same batch" if with_bwd else ""), "B": w.B, "H": w.H,
                        "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult,
                        "schedule": args.schedule,
+                       "f32_path": args.f32_path if w.dtype == "f32" else None,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
                        "l2": l2_note(w, qd)},
@@ -376,7 +397,8 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": K * ((-(-w.N // 128) + 1) if key_major else (1 + (3 if with_bwd else 0))),
+            "gpu_launches": K * ((-(-w.N // 128) + 1) if key_major else 4 if tf32x3 else
+                                 (1 + (3 if with_bwd else 0))),
             "clocks": clocks,
         }
         print(json.dumps(line))

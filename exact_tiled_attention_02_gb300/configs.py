@@ -62,15 +62,18 @@ WORKLOADS = {
 }
 
 
-def custom_workload(spec: str) -> Workload:
-    """A bf16 workload of another shape, from ``"B,H,N,d[,window[,qk_mult]]"``.
-    It has index 0, so its inputs are drawn with seed -1."""
+def custom_workload(spec: str, dtype: str = "bf16") -> Workload:
+    """A workload of another shape, from ``"B,H,N,d[,window[,qk_mult]]"``, in
+    ``dtype`` ("bf16" or "f32").  It has index 0, so its inputs are drawn with
+    seed -1."""
+    if dtype not in ("bf16", "f32"):
+        raise ValueError("dtype must be bf16 or f32")
     parts = [p.strip() for p in spec.split(",")]
     if not 4 <= len(parts) <= 6:
         raise ValueError("shape must be B,H,N,d[,window[,qk_mult]]")
     B, H, N, d = (int(x) for x in parts[:4])
     window = int(parts[4]) if len(parts) > 4 else 0
     qk = float(parts[5]) if len(parts) > 5 else 1.0
-    name = f"custom_bf16_b{B}_h{H}_n{N}_d{d}" + (f"_w{window}" if window > 0 else "") + \
+    name = f"custom_{dtype}_b{B}_h{H}_n{N}_d{d}" + (f"_w{window}" if window > 0 else "") + \
         (f"_qk{qk:g}" if qk != 1.0 else "")
-    return Workload(0, name, B, H, N, d, "bf16", window=window, qk_mult=qk, passes=("fwd", "bwd"))
+    return Workload(0, name, B, H, N, d, dtype, window=window, qk_mult=qk, passes=("fwd", "bwd"))
