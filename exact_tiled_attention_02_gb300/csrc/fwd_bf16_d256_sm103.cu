@@ -39,7 +39,6 @@ namespace {
 
 using namespace sm103;
 
-constexpr int D = 256;
 constexpr int BR = kFwdBlockRows;  // 128 query rows per CTA
 constexpr int BC = kFwdBlockCols;  // 128 keys per K/V tile
 constexpr int kThreads = 192;
@@ -47,20 +46,29 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
 constexpr int BOX_BYTES = 128 * 128;           // a [128 rows][64 columns] bf16 box, 128-byte swizzled
 constexpr int CHUNK_BYTES = 2 * BOX_BYTES;     // 128 rows x 128 columns
-constexpr int Q_BYTES = (D / 64) * BOX_BYTES;  // 64 KB
-constexpr int NCHUNK = 5;                      // ring depth
-constexpr int OFF_Q = 0;
-constexpr int OFF_RING = OFF_Q + Q_BYTES;
-constexpr int OFF_BAR = OFF_RING + NCHUNK * CHUNK_BYTES;
-// q_full, full[NCHUNK], empty[NCHUNK], s_full[2], p_full[2], o_done, drain
-constexpr int NBAR = 1 + 2 * NCHUNK + 6;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+// D = 256 is the one instantiated.  D = 128 also fits (a six-chunk ring); it
+// was measured as the single-query-tile point of the d = 128 tile-shape sweep
+// and lost to the two-tile kernel of fwd_bf16_sm103.cu by 8-12%.
+template <int D>
+struct Cfg1 {
+  static constexpr int CH = D / 128;                 // chunks per K or V tile
+  static constexpr int Q_BYTES = (D / 64) * BOX_BYTES;
+  static constexpr int NCHUNK = D == 256 ? 5 : 6;    // ring depth
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = OFF_Q + Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NCHUNK * CHUNK_BYTES;
+  // q_full, full[NCHUNK], empty[NCHUNK], s_full[2], p_full[2], o_done, drain
+  static constexpr int NBAR = 1 + 2 * NCHUNK + 6;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
 // Lazy rescaling threshold (log2 units), as in the d <= 128 kernel.
 constexpr float kRescaleThreshold = 8.0f;
 
+template <int NCHUNK>
 struct Bars {
   uint32_t base;
   __device__ uint32_t q_full() const { return base; }
@@ -75,10 +83,13 @@ struct Bars {
   __device__ uint32_t drain() const { return base + 8 * (6 + 2 * NCHUNK); }
 };
 
-template <bool WIN>
+template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_d256_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                                   const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
+  using C = Cfg1<D>;
+  constexpr int NCHUNK = C::NCHUNK, Q_BYTES = C::Q_BYTES, SMEM_USED = C::SMEM_USED, SMEM_BYTES = C::SMEM_BYTES;
+  constexpr int OFF_Q = C::OFF_Q, OFF_RING = C::OFF_RING, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -89,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t sQ = sb + OFF_Q, sRing = sb + OFF_RING;
-  const Bars bar{sb + OFF_BAR};
+  const Bars<NCHUNK> bar{sb + OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   const WaitCtl wc{p.status, abort_flag, p.wait_ns};
@@ -144,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b = 0; b < D / 64; ++b) tma_load_3d(sQ + b * BOX_BYTES, &tmq, bar.q_full(), b * 64, i0, bh);
       int seq = 0;  // chunks issued
       bool ok = true;
-      // the two chunks (dimensions 0-127, 128-255) of K or V tile j
+      // the chunks (dimensions 0-127, 128-255, ...) of K or V tile j
       auto load_unit = [&](int j, bool is_v) {
         const int kv0 = (j_lo + j) * BC;
-        for (int half = 0; half < 2 && ok; ++half, ++seq) {
+        for (int half = 0; half < C::CH && ok; ++half, ++seq) {
           const int c = seq % NCHUNK;
           if (!mbar_wait_backoff(bar.empty(c), ((seq / NCHUNK) & 1) ^ 1, wc)) {
             ok = false;
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j % 2
         const uint32_t d_tm = tmem + 128 * (j & 1);
-        for (int half = 0; half < 2; ++half, ++seq) {
+        for (int half = 0; half < C::CH; ++half, ++seq) {
           int c;
           if (!wait_chunk(c)) return false;
           const uint32_t kbase = sRing + c * CHUNK_BYTES;
@@ -208,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar.p_full(j & 1), (j >> 1) & 1, wc)) return false;
         tc_fence_after();
         const uint32_t a_tm = tmem + 128 * (j & 1);
-        for (int half = 0; half < 2; ++half, ++seq) {
+        for (int half = 0; half < C::CH; ++half, ++seq) {
           int c;
           if (!wait_chunk(c)) return false;
           const uint32_t vbase = sRing + c * CHUNK_BYTES;
@@ -397,26 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool WIN>
+template <int D, bool WIN>
 cudaError_t launch_win(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
+  constexpr int SMEM_BYTES = Cfg1<D>::SMEM_BYTES;
   static bool configured = false;  // attribute set once per process
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_d256_sm103_kernel<WIN>,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_d256_sm103_kernel<D, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const long long grid = static_cast<long long>((p.N + BR - 1) / BR) * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_bf16_d256_sm103_kernel<WIN><<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
+  fa_fwd_bf16_d256_sm103_kernel<D, WIN><<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16_d256(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
-  if (p.d != D) return cudaErrorInvalidValue;
-  return p.window_r >= 0 ? launch_win<true>(p, m, s) : launch_win<false>(p, m, s);
+  if (p.d == 256) return p.window_r >= 0 ? launch_win<256, true>(p, m, s) : launch_win<256, false>(p, m, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

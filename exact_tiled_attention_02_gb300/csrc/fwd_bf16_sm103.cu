@@ -388,10 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 sl2 = make_float2(sl, sl), nref2 = make_float2(nref, nref);
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // P (bf16 pairs) over the first half of this tile's S columns, written in
-      // four groups of 16 columns as soon as each group is ready; S columns
+      // groups of 16 columns as soon as each group is ready; S columns
       // 32g..32g+31 were read above, before group g overwrites columns 16g..16g+15
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < BC / 32; ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
