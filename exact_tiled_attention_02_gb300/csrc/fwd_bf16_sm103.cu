@@ -15,7 +15,19 @@
 // end.  Score tiles live only in tensor memory; nothing of size N x N reaches
 // device memory.
 //
-// CTA = two 128-row query tiles (Q0, Q1) of one (batch, head); 384 threads:
+// Work item = two 128-row query tiles (Q0, Q1) of one (batch, head).  The
+// kernel is persistent: one CTA per SM (at most) takes items c, c + G,
+// c + 2G, ... (G = the grid), every barrier's phase counting across items, so
+// one item's start-up (loading Q and its first K/V tiles) overlaps the
+// previous item's last products and output:
+//   * the K/V ring runs on across items;
+//   * Q_t of the next item is loaded once the current item's last Q_t K^T has
+//     completed (the MMA warp commits q_empty(t) right after issuing it);
+//   * O is written from registers (16-byte stores, one row per thread), not
+//     staged in the Q buffer, which by then holds the next item's Q.
+// (Measured against one item per CTA: identical results bit for bit, 2.6% to
+// 7% faster on long key loops, 24% on the window-257 workload.)
+// 384 threads:
 //   warps 0-3  softmax for Q0: thread t owns row t of Q0 (TMEM lane t)
 //   warps 4-7  softmax for Q1: thread t owns row t of Q1 (TMEM lane t)
 //   warp  8    TMEM owner + tcgen05.mma issuer (one elected lane)
@@ -45,7 +57,7 @@ namespace {
 
 using namespace sm103;
 
-constexpr int BR = kFwdBlockRows;  // rows per query tile (two per CTA)
+constexpr int BR = kFwdBlockRows;  // rows per query tile (two per item)
 constexpr int BC = kFwdBlockCols;  // keys per K/V tile
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
@@ -69,17 +81,18 @@ template <int D>
 struct Cfg {
   static constexpr int DP = (D + 63) / 64 * 64;
   static constexpr int STAGES = (DP == 128) ? 2 : 3;
-  static constexpr int BOXES = DP / 64;         // 64-column (128-byte) boxes per row
-  static constexpr int Q_BYTES = BR * DP * 2;   // one query tile
-  static constexpr int KV_BYTES = BC * DP * 2;  // one K or one V tile
+  static constexpr int BOXES = DP / 64;
+  static constexpr int Q_BYTES = BR * DP * 2;
+  static constexpr int KV_BYTES = BC * DP * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // q_full[2], k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 2 + 3 * STAGES + 7;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  // q_full[2], q_empty[2], k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 4 + 3 * STAGES + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(D % 32 == 0 && DP <= 128, "tensor memory budget");
 };
@@ -88,69 +101,82 @@ template <int STAGES>
 struct Bars {
   uint32_t base;
   __device__ uint32_t q_full(int t) const { return base + 8 * t; }
-  __device__ uint32_t k_full(int s) const { return base + 8 * (2 + s); }
-  __device__ uint32_t v_full(int s) const { return base + 8 * (2 + STAGES + s); }
-  __device__ uint32_t kv_empty(int s) const { return base + 8 * (2 + 2 * STAGES + s); }
-  __device__ uint32_t s_full(int t) const { return base + 8 * (2 + 3 * STAGES + t); }
-  __device__ uint32_t p_full(int t) const { return base + 8 * (4 + 3 * STAGES + t); }
-  __device__ uint32_t o_done(int t) const { return base + 8 * (6 + 3 * STAGES + t); }
-  __device__ uint32_t drain() const { return base + 8 * (8 + 3 * STAGES); }
+  __device__ uint32_t q_empty(int t) const { return base + 8 * (2 + t); }
+  __device__ uint32_t k_full(int s) const { return base + 8 * (4 + s); }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (4 + STAGES + s); }
+  __device__ uint32_t kv_empty(int s) const { return base + 8 * (4 + 2 * STAGES + s); }
+  __device__ uint32_t s_full(int t) const { return base + 8 * (4 + 3 * STAGES + t); }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (6 + 3 * STAGES + t); }
+  __device__ uint32_t o_done(int t) const { return base + 8 * (8 + 3 * STAGES + t); }
+  __device__ uint32_t drain() const { return base + 8 * (10 + 3 * STAGES); }
 };
 
-// WIN: compiled for a local window (band masks, per-tile key ranges); the
-// unmasked instantiation carries none of that code.
+// The key tiles of one item: [j_lo, j_lo + ntiles), and each query tile's own
+// range as offsets into it (only in-band tiles when windowed).
+struct Item {
+  int bh, i0, j_lo, ntiles;
+  int lo[2], hi[2];
+};
+
+template <bool WIN>
+__device__ __forceinline__ Item decode_item(int item, int N, int r) {
+  Item w;
+  const int nqt = (N + 2 * BR - 1) / (2 * BR);
+  w.bh = item / nqt;
+  w.i0 = (item % nqt) * (2 * BR);
+  w.j_lo = 0;
+  int j_hi = (N + BC - 1) / BC;
+  if (WIN) {
+    w.j_lo = max(0, w.i0 - r) / BC;
+    j_hi = (min(N, w.i0 + 2 * BR + r) + BC - 1) / BC;
+  }
+  w.ntiles = j_hi - w.j_lo;
+  for (int t = 0; t < 2; ++t) {
+    w.lo[t] = 0;
+    w.hi[t] = w.ntiles;
+    const int row_lo = w.i0 + t * BR, row_hi = min(N, row_lo + BR) - 1;
+    if (WIN) {
+      if (row_lo >= N) {
+        w.hi[t] = 0;
+      } else {
+        w.lo[t] = max(0, row_lo - r) / BC - w.j_lo;
+        w.hi[t] = (min(N, row_hi + r + 1) + BC - 1) / BC - w.j_lo;
+      }
+    }
+  }
+  return w;
+}
+
 template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                             const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
+                                     const __grid_constant__ CUtensorMap tmv, const FwdParams p, int n_items) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sb = smem_u32(smem);
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  if (pad + C::SMEM_USED > static_cast<uint32_t>(C::SMEM_BYTES)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
   const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
   const Bars<C::STAGES> bar{sb + C::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const WaitCtl wc{p.status, abort_flag, p.wait_ns};
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
   const int r = WIN ? p.window_r : -1;
-  const int nqt = (N + 2 * BR - 1) / (2 * BR);
-  const int bh = blockIdx.x / nqt;
-  const int i0 = (blockIdx.x % nqt) * (2 * BR);  // first row of Q0; Q1 starts at i0 + BR
-
-  // key tiles the two query tiles need (only in-band tiles when windowed)
-  int j_lo = 0, j_hi = (N + BC - 1) / BC;
-  if (WIN) {
-    const int lo = max(0, i0 - r);
-    const int hi = min(N, i0 + 2 * BR + r);  // exclusive
-    j_lo = lo / BC;
-    j_hi = (hi + BC - 1) / BC;
-  }
-  const int ntiles = j_hi - j_lo;
-  // each query tile's own key-tile range, as offsets into [j_lo, j_hi): with a
-  // window, a tile skips the union's tiles that lie wholly outside its band
-  auto tile_range = [&](int t, int& lo, int& hi) {
-    lo = 0;
-    hi = ntiles;
-    const int row_lo = i0 + t * BR, row_hi = min(N, row_lo + BR) - 1;
-    if (WIN) {
-      if (row_lo >= N) {
-        hi = 0;  // no rows: nothing to compute or store
-      } else {
-        lo = max(0, row_lo - r) / BC - j_lo;
-        hi = (min(N, row_hi + r + 1) + BC - 1) / BC - j_lo;
-      }
-    }
-  };
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.q_empty(t), 1);
       mbar_init(bar.s_full(t), 1);
-      mbar_init(bar.p_full(t), 4);  // one arrive per softmax warp of the tile
+      mbar_init(bar.p_full(t), 4);
       mbar_init(bar.o_done(t), 1);
     }
     for (int s = 0; s < C::STAGES; ++s) {
@@ -180,38 +206,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tmq);
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
-      for (int t = 0; t < 2; ++t) {
-        mbar_arrive_expect_tx(bar.q_full(t), C::Q_BYTES);
+      bool ok = true;
+      int g = 0;         // ring slots issued so far (all items)
+      int nq = 0;        // items whose Q was issued
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++nq) {
+        const Item w = decode_item<WIN>(item, N, r);
+        for (int t = 0; t < 2; ++t) {
+          // the previous item's last Q_t K^T has completed
+          if (nq > 0 && !mbar_wait_backoff(bar.q_empty(t), (nq - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar.q_full(t), C::Q_BYTES);
 #pragma unroll
-        for (int b = 0; b < C::BOXES; ++b)
-          tma_load_3d(sQ + t * C::Q_BYTES + b * BR * 128, &tmq, bar.q_full(t), b * 64, i0 + t * BR, bh);
-      }
-      int issued = 0;
-      for (int it = 0; it < ntiles; ++it) {
-        const int st = it % C::STAGES;
-        const uint32_t ph = (it / C::STAGES) & 1;
-        if (!mbar_wait_backoff(bar.kv_empty(st), ph ^ 1, wc)) break;
-        const int kv0 = (j_lo + it) * BC;
-        mbar_arrive_expect_tx(bar.k_full(st), C::KV_BYTES);
+          for (int b = 0; b < C::BOXES; ++b)
+            tma_load_3d(sQ + t * C::Q_BYTES + b * BR * 128, &tmq, bar.q_full(t), b * 64, w.i0 + t * BR, w.bh);
+        }
+        for (int it = 0; ok && it < w.ntiles; ++it, ++g) {
+          const int st = g % C::STAGES;
+          if (!mbar_wait_backoff(bar.kv_empty(st), ((g / C::STAGES) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          const int kv0 = (w.j_lo + it) * BC;
+          mbar_arrive_expect_tx(bar.k_full(st), C::KV_BYTES);
 #pragma unroll
-        for (int b = 0; b < C::BOXES; ++b)
-          tma_load_3d(sK + st * C::KV_BYTES + b * BC * 128, &tmk, bar.k_full(st), b * 64, kv0, bh);
-        mbar_arrive_expect_tx(bar.v_full(st), C::KV_BYTES);
+          for (int b = 0; b < C::BOXES; ++b)
+            tma_load_3d(sK + st * C::KV_BYTES + b * BC * 128, &tmk, bar.k_full(st), b * 64, kv0, w.bh);
+          mbar_arrive_expect_tx(bar.v_full(st), C::KV_BYTES);
 #pragma unroll
-        for (int b = 0; b < C::BOXES; ++b)
-          tma_load_3d(sV + st * C::KV_BYTES + b * BC * 128, &tmv, bar.v_full(st), b * 64, kv0, bh);
-        issued = it + 1;
+          for (int b = 0; b < C::BOXES; ++b)
+            tma_load_3d(sV + st * C::KV_BYTES + b * BC * 128, &tmv, bar.v_full(st), b * 64, kv0, w.bh);
+        }
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory is released
         WaitCtl drain{nullptr, nullptr, wc.limit_ns};
-        mbar_wait(bar.q_full(0), 0, drain);
-        mbar_wait(bar.q_full(1), 0, drain);
-        for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
-          const int st = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          mbar_wait(bar.k_full(st), ph, drain);
-          mbar_wait(bar.v_full(st), ph, drain);
+        if (nq > 0) {
+          mbar_wait(bar.q_full(0), (nq - 1) & 1, drain);
+          mbar_wait(bar.q_full(1), (nq - 1) & 1, drain);
+        }
+        for (int s = max(0, g - C::STAGES); s < g; ++s) {
+          mbar_wait(bar.k_full(s % C::STAGES), (s / C::STAGES) & 1, drain);
+          mbar_wait(bar.v_full(s % C::STAGES), (s / C::STAGES) & 1, drain);
         }
       }
     }
@@ -219,10 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BR, BC, 0, 0);  // Q: K-major, K tile: K-major
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, C::DP, 0, 1);  // P (TMEM), V tile: MN-major
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BR, BC, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, C::DP, 0, 1);
+      int g0 = 0;               // ring slot of the current item's first key tile
+      int cnt[2] = {0, 0};      // key tiles each query tile has processed (all items)
+      int nq = 0;               // items started
+      int last[2] = {0, 0};     // index of each tile's last key tile in the current item
       auto issue_s = [&](int t, int it) {  // S_t = Q_t K_it^T
-        const uint32_t kbase = sK + (it % C::STAGES) * C::KV_BYTES;
+        const uint32_t kbase = sK + ((g0 + it) % C::STAGES) * C::KV_BYTES;
         const uint32_t qbase = sQ + t * C::Q_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -232,91 +273,111 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(kbase + offk, 16, 1024), idesc_qk, kk > 0);
         }
         mma_commit(bar.s_full(t));
+        if (it == last[t]) mma_commit(bar.q_empty(t));  // Q_t is free once this product completes
       };
       auto issue_pv = [&](int t, int it, bool first) {  // O_t (+)= P_t V_it
-        const uint32_t vbase = sV + (it % C::STAGES) * C::KV_BYTES;
+        const uint32_t vbase = sV + ((g0 + it) % C::STAGES) * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
           mma_bf16_ts(tmem + kTmemO + t * 128, tmem + kTmemS + t * 128 + kk * 8,
                       sdesc_sw128(vbase + kk * 16 * 128, BC * 128, 1024), idesc_pv, (!first || kk > 0));
         mma_commit(bar.o_done(t));
       };
-      auto wait_k = [&](int it) { return mbar_wait(bar.k_full(it % C::STAGES), (it / C::STAGES) & 1, wc); };
-      if constexpr (!WIN) {
-        // both tiles take every key tile: PV0(j), S0(j+1), PV1(j), release, S1(j+1)
-        bool ok = mbar_wait(bar.q_full(0), 0, wc) && wait_k(0);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, 0);
-          ok = mbar_wait(bar.q_full(1), 0, wc);
+      auto wait_k = [&](int it) {
+        const int g = g0 + it;
+        return mbar_wait(bar.k_full(g % C::STAGES), (g / C::STAGES) & 1, wc);
+      };
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++nq) {
+        const Item w = decode_item<WIN>(item, N, r);
+        ok = mbar_wait(bar.q_full(0), nq & 1, wc) && mbar_wait(bar.q_full(1), nq & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          last[t] = w.hi[t] - 1;
+          if (w.lo[t] >= w.hi[t]) mma_commit(bar.q_empty(t));  // no product reads Q_t in this item
+        }
+        if (!WIN) {
+          // both tiles take every key tile: PV0(j), S0(j+1), PV1(j), release, S1(j+1)
+          ok = wait_k(0);
           if (ok) {
             tc_fence_after();
+            issue_s(0, 0);
             issue_s(1, 0);
           }
-        }
-        for (int it = 0; ok && it < ntiles; ++it) {
-          const int st = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          const bool more = it + 1 < ntiles;
-          if (!mbar_wait(bar.v_full(st), ph, wc)) break;
-          if (!mbar_wait(bar.p_full(0), it & 1, wc)) break;
-          tc_fence_after();
-          issue_pv(0, it, it == 0);
-          if (more) {
-            if (!wait_k(it + 1)) break;
-            tc_fence_after();
-            issue_s(0, it + 1);
-          }
-          if (!mbar_wait(bar.p_full(1), it & 1, wc)) break;
-          tc_fence_after();
-          issue_pv(1, it, it == 0);
-          mma_commit(bar.kv_empty(st));  // before S1(j+1): a commit waits for every earlier MMA
-          if (more) issue_s(1, it + 1);
-        }
-      } else {
-        // windowed: each tile only over its own key range
-        int t_lo[2], t_hi[2];
-        tile_range(0, t_lo[0], t_hi[0]);
-        tile_range(1, t_lo[1], t_hi[1]);
-        bool ok = true;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || t_lo[t] >= t_hi[t]) continue;
-          ok = mbar_wait(bar.q_full(t), 0, wc) && wait_k(t_lo[t]);
-          if (ok) {
-            tc_fence_after();
-            issue_s(t, t_lo[t]);
-          }
-        }
-        int cnt[2] = {0, 0};
-        for (int it = 0; ok && it < ntiles; ++it) {
-          const int st = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          if (!mbar_wait(bar.v_full(st), ph, wc)) break;
-          bool k_next = false;  // K tile it+1 known to be resident
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!ok || it < t_lo[t] || it >= t_hi[t]) continue;
-            if (!mbar_wait(bar.p_full(t), cnt[t] & 1, wc)) {
+          for (int it = 0; ok && it < w.ntiles; ++it) {
+            const int g = g0 + it;
+            const int st = g % C::STAGES;
+            const bool more = it + 1 < w.ntiles;
+            if (!mbar_wait(bar.v_full(st), (g / C::STAGES) & 1, wc) || !mbar_wait(bar.p_full(0), (cnt[0] + it) & 1, wc)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_pv(t, it, cnt[t] == 0);
-            ++cnt[t];
-            // release the K/V slot right after the last product that reads V_it
-            // (a commit waits for every earlier MMA, so it must precede S_t(it+1))
-            if (t == 1 || it < t_lo[1] || it >= t_hi[1]) mma_commit(bar.kv_empty(st));
-            if (it + 1 < t_hi[t]) {
-              if (!k_next && !(k_next = wait_k(it + 1))) {
+            issue_pv(0, it, it == 0);
+            if (more) {
+              if (!wait_k(it + 1)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_s(t, it + 1);
+              issue_s(0, it + 1);
+            }
+            if (!mbar_wait(bar.p_full(1), (cnt[1] + it) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(1, it, it == 0);
+            mma_commit(bar.kv_empty(st));  // before S1(j+1): a commit waits for every earlier MMA
+            if (more) issue_s(1, it + 1);
+          }
+          cnt[0] += w.ntiles;
+          cnt[1] += w.ntiles;
+        } else {
+          // windowed: each tile only over its own key range
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || w.lo[t] >= w.hi[t]) continue;
+            ok = wait_k(w.lo[t]);
+            if (ok) {
+              tc_fence_after();
+              issue_s(t, w.lo[t]);
             }
           }
+          int c[2] = {0, 0};
+          for (int it = 0; ok && it < w.ntiles; ++it) {
+            const int g = g0 + it;
+            const int st = g % C::STAGES;
+            if (!mbar_wait(bar.v_full(st), (g / C::STAGES) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            bool k_next = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok || it < w.lo[t] || it >= w.hi[t]) continue;
+              if (!mbar_wait(bar.p_full(t), (cnt[t] + c[t]) & 1, wc)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_pv(t, it, c[t] == 0);
+              ++c[t];
+              if (t == 1 || it < w.lo[1] || it >= w.hi[1]) mma_commit(bar.kv_empty(st));
+              if (it + 1 < w.hi[t]) {
+                if (!k_next && !(k_next = wait_k(it + 1))) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_s(t, it + 1);
+              }
+            }
+          }
+          cnt[0] += c[0];
+          cnt[1] += c[1];
         }
+        g0 += w.ntiles;
       }
       // every MMA this thread issued must finish before tensor memory is freed
       mma_commit(bar.drain());
@@ -326,157 +387,139 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // -------------------------------------------------------------- softmax
-    const int t = warp >> 2;             // query tile of this warpgroup
-    const int row = threadIdx.x & 127;   // row within the tile == TMEM lane
-    const int qi = i0 + t * BR + row;
+    const int t = warp >> 2;
+    const int row = threadIdx.x & 127;
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t tS = tl + kTmemS + t * 128, tO = tl + kTmemO + t * 128;
     const float sl = p.scale_log2;
-    const int qlo = i0 + t * BR, qhi = qlo + BR - 1;  // rows of this tile
-    float m_ref = -INFINITY;  // running reference maximum, log2 units of scaled scores
-    float l = 0.f;
     bool ok = true;
-    // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
+    int n = 0;  // key tiles this warpgroup has processed (all items)
     auto warp_wait = [&](uint32_t bar_addr, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
     };
-    int my_lo = 0, my_hi = ntiles;
-    if constexpr (WIN) tile_range(t, my_lo, my_hi);
-    for (int it = my_lo; it < my_hi; ++it) {
-      const int n = it - my_lo;  // tiles this warpgroup has processed
-      if (!warp_wait(bar.s_full(t), n & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[BC];
-#pragma unroll
-      for (int c = 0; c < BC / 32; ++c) tmem_ld_32x32b_x32(tS + c * 32, &sr[c * 32]);
-      tmem_wait_ld();
-
-      float s[BC];
-#pragma unroll
-      for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
-      const int kv0 = (j_lo + it) * BC;
-      const bool edge = (kv0 + BC > N) || (WIN && !(kv0 >= qhi - r && kv0 + BC - 1 <= qlo + r));
-      if (edge) {
-        // the visible keys of row qi form one contiguous column range [lo, hi)
-        int lo = 0, hi = min(BC, N - kv0);
-        if (WIN) {
-          lo = max(lo, qi - r - kv0);
-          hi = min(hi, qi + r + 1 - kv0);
-        }
-        const unsigned span = hi > lo ? static_cast<unsigned>(hi - lo) : 0u;
-#pragma unroll
-        for (int c = 0; c < BC; ++c) s[c] = (static_cast<unsigned>(c - lo) < span) ? s[c] : -INFINITY;
-      }
-      // row maximum: four independent chains of three-input max
-      float mx[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) mx[a] = fmaxf(s[a], s[a + 4]);
-#pragma unroll
-      for (int c = 8; c < BC; c += 8)
-#pragma unroll
-        for (int a = 0; a < 4; ++a) mx[a] = fmax3(mx[a], s[c + a], s[c + 4 + a]);
-      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl;
-      float alpha = 1.f;
-      if (mt > m_ref + kRescaleThreshold) {
-        alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
-        m_ref = mt;
-      }
-      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      const float2 sl2 = make_float2(sl, sl), nref2 = make_float2(nref, nref);
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      // P (bf16 pairs) over the first half of this tile's S columns, written in
-      // groups of 16 columns as soon as each group is ready; S columns
-      // 32g..32g+31 were read above, before group g overwrites columns 16g..16g+15
-#pragma unroll
-      for (int g = 0; g < BC / 32; ++g) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int e = 32 * g + 2 * c;
-          const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), sl2, nref2);
-          const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          rs[c & 3] = __fadd2_rn(rs[c & 3], pv);
-          pk[c] = pack_bf16x2(pv.x, pv.y);
-        }
-        tmem_st_32x32b_x16(tS + 16 * g, pk);
-      }
-      const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y) + (rs[2].x + rs[2].y) + (rs[3].x + rs[3].y);
-      // O may be rescaled only once the previous P V into it has completed
-      if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
-          tmem_wait_st();
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const Item w = decode_item<WIN>(item, N, r);
+      const int qi = w.i0 + t * BR + row;
+      const int qlo = w.i0 + t * BR, qhi = qlo + BR - 1;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int it = w.lo[t]; it < w.hi[t]; ++it, ++n) {
+        if (!warp_wait(bar.s_full(t), n & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // one TMEM round trip: all D columns loaded, scaled, stored back
-        uint32_t o[D];
+        uint32_t sr[BC];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld_32x32b_x32(tO + c * 32, &o[c * 32]);
+        for (int c = 0; c < BC / 32; ++c) tmem_ld_32x32b_x32(tS + c * 32, &sr[c * 32]);
         tmem_wait_ld();
-        const float2 a2 = make_float2(alpha, alpha);
+        float s[BC];
 #pragma unroll
-        for (int e = 0; e < D; e += 2) {
-          const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
-          o[e] = __float_as_uint(v.x);
-          o[e + 1] = __float_as_uint(v.y);
+        for (int c = 0; c < BC; ++c) s[c] = __uint_as_float(sr[c]);
+        const int kv0 = (w.j_lo + it) * BC;
+        const bool edge = (kv0 + BC > N) || (WIN && !(kv0 >= qhi - r && kv0 + BC - 1 <= qlo + r));
+        if (edge) {
+          int lo = 0, hi = min(BC, N - kv0);
+          if (WIN) {
+            lo = max(lo, qi - r - kv0);
+            hi = min(hi, qi + r + 1 - kv0);
+          }
+          const unsigned span = hi > lo ? static_cast<unsigned>(hi - lo) : 0u;
+#pragma unroll
+          for (int c = 0; c < BC; ++c) s[c] = (static_cast<unsigned>(c - lo) < span) ? s[c] : -INFINITY;
         }
+        float mx[4];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_st_32x32b_x32(tO + c * 32, &o[c * 32]);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full(t));
-      l = l * alpha + rsum;
-    }
-
-    // ------------------------------------------------------------ epilogue
-    const bool have = ok && my_lo < my_hi && warp_wait(bar.o_done(t), (my_hi - my_lo - 1) & 1);
-    // the tile's Q buffer is idle once its last P V has completed: stage the
-    // bf16 O tile there, swizzled like the TMA layout of Q
-    const uint32_t sO = sQ + t * C::Q_BYTES;
-    if (have) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
+        for (int a = 0; a < 4; ++a) mx[a] = fmaxf(s[a], s[a + 4]);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tO + c * 32, o);
-        tmem_wait_ld();
+        for (int c = 8; c < BC; c += 8)
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int c16 = c * 4 + q4;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
-                               __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-          const uint32_t addr = sO + (c16 >> 3) * (BR * 128) + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
-          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          for (int a = 0; a < 4; ++a) mx[a] = fmax3(mx[a], s[c + a], s[c + 4 + a]);
+        const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl;
+        float alpha = 1.f;
+        if (mt > m_ref + kRescaleThreshold) {
+          alpha = ex2_approx(m_ref - mt);
+          m_ref = mt;
         }
-      }
-      if (p.lse != nullptr && qi < N) {
-        const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        p.lse[static_cast<size_t>(bh) * N + qi] = (mref + __log2f(l)) * 0.69314718055994531f;
-      }
-    }
-    tc_fence_before();
-    named_bar_sync(1 + t, 128);  // reached by all four warps of the tile on every path
-    if (have && !*abort_flag) {
-      // coalesced 128-bit stores: consecutive threads write consecutive 16-byte chunks
-      constexpr int CHUNKS = D / 8;
-      const int row0 = i0 + t * BR;
-      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * N + row0) * D * 2;
-      for (int idx = row; idx < BR * CHUNKS; idx += 128) {
-        const int rr = idx / CHUNKS, c16 = idx % CHUNKS;
-        if (row0 + rr < N) {
-          const uint4 val = ld_shared_v4(sO + (c16 >> 3) * (BR * 128) + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4));
-          st_global_v4(obase + static_cast<size_t>(rr) * D * 2 + c16 * 16, val);
+        const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const float2 sl2 = make_float2(sl, sl), nref2 = make_float2(nref, nref);
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int gq = 0; gq < BC / 32; ++gq) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int e = 32 * gq + 2 * c;
+            const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), sl2, nref2);
+            const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            rs[c & 3] = __fadd2_rn(rs[c & 3], pv);
+            pk[c] = pack_bf16x2(pv.x, pv.y);
+          }
+          tmem_st_32x32b_x16(tS + 16 * gq, pk);
         }
+        const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y) + (rs[2].x + rs[2].y) + (rs[3].x + rs[3].y);
+        // O may be rescaled only once this item's previous P V into it has
+        // completed (the first tile of an item starts a fresh O)
+        if (it > w.lo[t] && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
+            tmem_wait_st();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t o[D];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld_32x32b_x32(tO + c * 32, &o[c * 32]);
+          tmem_wait_ld();
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int e = 0; e < D; e += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+            o[e] = __float_as_uint(v.x);
+            o[e + 1] = __float_as_uint(v.y);
+          }
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_st_32x32b_x32(tO + c * 32, &o[c * 32]);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.p_full(t));
+        l = l * alpha + rsum;
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ output
+      // wait for this item's last P V (the next item's first P V into O needs
+      // this warpgroup's first P of that item, so it cannot have started)
+      if (w.lo[t] < w.hi[t]) {
+        if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(w.bh) * N + qi) * D * 2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + c * 32, o);
+          tmem_wait_ld();
+          if (qi < N && !*abort_flag) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+              st_global_v4(orow + (c * 4 + q4) * 16, v);
+            }
+          }
+        }
+        if (p.lse != nullptr && qi < N) {
+          const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
+          p.lse[static_cast<size_t>(w.bh) * N + qi] = (mref + __log2f(l)) * 0.69314718055994531f;
+        }
+        tc_fence_before();
       }
     }
   }
@@ -489,20 +532,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 template <int D, bool WIN>
 cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
   using C = Cfg<D>;
-  static bool configured = false;  // attribute set once per process (one device per process in practice)
+  static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_sm103_kernel<D, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const long long nqt = (p.N + 2 * BR - 1) / (2 * BR);
-  const long long grid = nqt * p.BH;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_bf16_sm103_kernel<D, WIN><<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
+  const long long items = static_cast<long long>((p.N + 2 * BR - 1) / (2 * BR)) * p.BH;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  fa_fwd_bf16_sm103_kernel<D, WIN><<<grid, kThreads, C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p,
+                                                                                 static_cast<int>(items));
   return cudaGetLastError();
 }
 
