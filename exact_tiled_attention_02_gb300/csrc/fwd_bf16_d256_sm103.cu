@@ -201,14 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int half = 0; half < C::CH; ++half, ++seq) {
           int c;
           if (!wait_chunk(c)) return false;
-          const uint32_t kbase = sRing + c * CHUNK_BYTES;
+          // descriptors built once, advanced by their address field per K-step
+          const uint64_t dq = sdesc_sw128(sQ, 16, 1024), dk = sdesc_sw128(sRing + c * CHUNK_BYTES, 16, 1024);
 #pragma unroll
           for (int k8 = 0; k8 < 8; ++k8) {  // 16 dimensions per step; 8 steps per chunk
             const int kk = half * 8 + k8;
             const uint32_t offq = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
             const uint32_t offk = (k8 >> 2) * BOX_BYTES + (k8 & 3) * 32;
-            mma_bf16_ss(d_tm, sdesc_sw128(sQ + offq, 16, 1024), sdesc_sw128(kbase + offk, 16, 1024), idesc_qk,
-                        kk > 0);
+            mma_bf16_ss(d_tm, dq + (offq >> 4), dk + (offk >> 4), idesc_qk, kk > 0);
           }
           mma_commit(bar.empty(c));
         }
@@ -222,11 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int half = 0; half < C::CH; ++half, ++seq) {
           int c;
           if (!wait_chunk(c)) return false;
-          const uint32_t vbase = sRing + c * CHUNK_BYTES;
+          const uint64_t dv = sdesc_sw128(sRing + c * CHUNK_BYTES, BOX_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < BC / 16; ++kk)
-            mma_bf16_ts(tmem + kTmemO + 128 * half, a_tm + kk * 8, sdesc_sw128(vbase + kk * 16 * 128, BOX_BYTES, 1024),
-                        idesc_pv, (j > 0 || kk > 0));
+            mma_bf16_ts(tmem + kTmemO + 128 * half, a_tm + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv,
+                        (j > 0 || kk > 0));
           mma_commit(bar.empty(c));
         }
         mma_commit(bar.o_done());

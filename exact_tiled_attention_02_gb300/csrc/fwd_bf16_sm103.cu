@@ -263,24 +263,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nq = 0;               // items started
       int last[2] = {0, 0};     // index of each tile's last key tile in the current item
       auto issue_s = [&](int t, int it) {  // S_t = Q_t K_it^T
-        const uint32_t kbase = sK + ((g0 + it) % C::STAGES) * C::KV_BYTES;
-        const uint32_t qbase = sQ + t * C::Q_BYTES;
+        // descriptors built once per tile, advanced by their address field
+        // (16-byte units) per K-step: the MMA warp shares its SM
+        // sub-partition with two softmax warps, and rebuilding both 64-bit
+        // descriptors for every instruction made issuing slower than the
+        // tensor core (measured: 3-4% on long key loops).  Every sum is
+        // still a shared-memory address below 256 KB, so the 14-bit field
+        // never carries into the neighbouring offset fields.
+        const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sK + ((g0 + it) % C::STAGES) * C::KV_BYTES, 16, 1024);
+        const uint32_t dt = tmem + kTmemS + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offq = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
           const uint32_t offk = (kk >> 2) * (BC * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kTmemS + t * 128, sdesc_sw128(qbase + offq, 16, 1024),
-                      sdesc_sw128(kbase + offk, 16, 1024), idesc_qk, kk > 0);
+          mma_bf16_ss(dt, dq + (offq >> 4), dk + (offk >> 4), idesc_qk, kk > 0);
         }
         mma_commit(bar.s_full(t));
         if (it == last[t]) mma_commit(bar.q_empty(t));  // Q_t is free once this product completes
       };
       auto issue_pv = [&](int t, int it, bool first) {  // O_t (+)= P_t V_it
-        const uint32_t vbase = sV + ((g0 + it) % C::STAGES) * C::KV_BYTES;
+        const uint64_t dv = sdesc_sw128(sV + ((g0 + it) % C::STAGES) * C::KV_BYTES, BC * 128, 1024);
+        const uint32_t dt = tmem + kTmemO + t * 128, at = tmem + kTmemS + t * 128;
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ts(tmem + kTmemO + t * 128, tmem + kTmemS + t * 128 + kk * 8,
-                      sdesc_sw128(vbase + kk * 16 * 128, BC * 128, 1024), idesc_pv, (!first || kk > 0));
+          mma_bf16_ts(dt, at + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0));
         mma_commit(bar.o_done(t));
       };
       auto wait_k = [&](int it) {
