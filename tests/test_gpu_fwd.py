@@ -84,6 +84,10 @@ BF16_CASES = [
     (1, 2, 1000, 64, 257, 1.0),
     (1, 1, 640, 128, 257, 8.0),
     (1, 1, 257, 128, 513, 1.0),
+    # more work items than SMs, so each CTA walks several items and the two
+    # query tiles pass the d = 64 output staging tile back and forth; the last
+    # item of every head has its second query tile wholly past N
+    (1, 48, 1100, 64, 0, 1.0),
     (1, 1, 1, 96, 0, 1.0),
     (1, 2, 129, 96, 0, 1.0),
     (2, 1, 513, 96, 0, 8.0),
