@@ -39,6 +39,38 @@ namespace {
 
 using namespace sm103;
 
+// Shared-memory descriptor split in its two 32-bit words: the start address
+// (bits 0-13) lives in the low word, so advancing it within one chunk is a
+// 32-bit add (the field cannot carry: every address is below 256 KB), one
+// instruction fewer per operand than a 64-bit add on the MMA warp (measured:
+// 1.2-1.8% faster).
+struct Desc2 {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc2 desc2(uint64_t d) {
+  return Desc2{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, Desc2 a, uint32_t a_off, Desc2 b, uint32_t b_off,
+                                        uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .b64 da, db;\n"
+      "mov.b64 da, {%1, %2};\nmov.b64 db, {%3, %4};\n"
+      "setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + a_off), "r"(a.hi), "r"(b.lo + b_off), "r"(b.hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, Desc2 b, uint32_t b_off, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .b64 db;\n"
+      "mov.b64 db, {%2, %3};\n"
+      "setp.ne.b32 p, %5, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off), "r"(b.hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 constexpr int BR = kFwdBlockRows;  // 128 query rows per CTA
 constexpr int BC = kFwdBlockCols;  // 128 keys per K/V tile
 constexpr int kThreads = 192;
@@ -208,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kk = half * 8 + k8;
             const uint32_t offq = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
             const uint32_t offk = (k8 >> 2) * BOX_BYTES + (k8 & 3) * 32;
-            mma_bf16_ss(d_tm, dq + (offq >> 4), dk + (offk >> 4), idesc_qk, kk > 0);
+            mma_ss2(d_tm, desc2(dq), offq >> 4, desc2(dk), offk >> 4, idesc_qk, kk > 0);
           }
           mma_commit(bar.empty(c));
         }
@@ -225,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dv = sdesc_sw128(sRing + c * CHUNK_BYTES, BOX_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < BC / 16; ++kk)
-            mma_bf16_ts(tmem + kTmemO + 128 * half, a_tm + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv,
+            mma_ts2(tmem + kTmemO + 128 * half, a_tm + kk * 8, desc2(dv), (kk * 16 * 128) >> 4, idesc_pv,
                         (j > 0 || kk > 0));
           mma_commit(bar.empty(c));
         }

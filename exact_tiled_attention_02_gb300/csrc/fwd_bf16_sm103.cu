@@ -71,6 +71,40 @@ constexpr uint32_t kTmemO = 256;  // + 128 * tile
 // 3.7e-4 at 2^8 to 6.1e-4 at 2^64.)
 constexpr float kRescaleThreshold = 8.0f;
 
+// Shared-memory descriptor split in its two 32-bit words: the start address
+// (bits 0-13) lives in the low word, so advancing it within one tile is a
+// 32-bit add (the field cannot carry: every address is below 256 KB), one
+// instruction fewer per operand than a 64-bit add on the MMA warp, which
+// shares its SM sub-partition with two softmax warps.  Measured: 2.0-2.4%
+// faster at d = 128, 1.2% at d = 96; at d = 64 the 64-bit form measured
+// 2.4% faster, so that instantiation keeps it.
+struct Desc2 {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc2 desc2(uint64_t d) {
+  return Desc2{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, Desc2 a, uint32_t a_off, Desc2 b, uint32_t b_off,
+                                        uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .b64 da, db;\n"
+      "mov.b64 da, {%1, %2};\nmov.b64 db, {%3, %4};\n"
+      "setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + a_off), "r"(a.hi), "r"(b.lo + b_off), "r"(b.hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, Desc2 b, uint32_t b_off, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .b64 db;\n"
+      "mov.b64 db, {%2, %3};\n"
+      "setp.ne.b32 p, %5, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off), "r"(b.hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // D = 64, 96 or 128.  Tiles in shared memory are DP = D rounded up to a
 // multiple of 64 columns wide (whole 128-byte swizzle atoms); for D = 96 the
 // TMA zero-fills columns 96..127.  Q K^T contracts over the D real columns
@@ -287,7 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offq = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
           const uint32_t offk = (kk >> 2) * (BC * 128) + (kk & 3) * 32;
-          mma_bf16_ss(dt, dq + (offq >> 4), dk + (offk >> 4), idesc_qk, kk > 0);
+          if constexpr (D != 64)
+            mma_ss2(dt, desc2(dq), offq >> 4, desc2(dk), offk >> 4, idesc_qk, kk > 0);
+          else
+            mma_bf16_ss(dt, dq + (offq >> 4), dk + (offk >> 4), idesc_qk, kk > 0);
         }
         mma_commit(bar.s_full(t));
         if (it == last[t]) mma_commit(bar.q_empty(t));  // Q_t is free once this product completes
@@ -297,7 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dt = tmem + kTmemO + t * 128, at = tmem + kTmemS + t * 128;
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ts(dt, at + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0));
+          if constexpr (D != 64)
+            mma_ts2(dt, at + kk * 8, desc2(dv), (kk * 16 * 128) >> 4, idesc_pv, (!first || kk > 0));
+          else
+            mma_bf16_ts(dt, at + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0));
         mma_commit(bar.o_done(t));
       };
       auto wait_k = [&](int it) {
