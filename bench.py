@@ -371,7 +371,7 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(fa, w, q, k, v, do, with_bwd, dev, min(K, 10), pg, fwd_fn)
+        e2e = run_e2e(fa, w, q, k, v, do, with_bwd, dev, K, pg, fwd_fn)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -415,7 +415,9 @@ def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg, fwd_fn=None):
     with the compute of the neighbouring steps: step i+1's inputs go up while
     step i computes, and step i-1's results come down meanwhile (two device
     buffer sets; events order every reuse).  The timed region starts before
-    step 0's upload and ends after the last step's download."""
+    step 0's upload and ends after the last step's download, and spans the
+    same number of steps as the kernel timing, so the one upload and one
+    download that nothing overlaps are spread over as many steps."""
     import torch
 
     fwd = fwd_fn or fa.fa_fwd
