@@ -38,8 +38,12 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;  // [B,H,N,d] fp32 workspace
-  float* lse2;    // [B,H,Npad] fp32 workspace: -lse_i * log2(e) (-inf in padding rows), Npad = N rounded up to 128
-  float* dsum;    // [B,H,Npad] fp32 workspace: -D_i = -sum_k dO_ik O_ik (0 in padding rows)
+  // [B,H,Npad] workspace rows, Npad = N rounded up to 128.  d = 96, 128: fp32
+  // -lse_i * log2(e) (-inf in padding rows) and -D_i = -sum_k dO_ik O_ik (0 in
+  // padding rows).  d = 64: 16-byte rows of three bf16 terms of -lse_i / scale
+  // (-1e30 in padding rows) and of -D_i (0), then five zeros.
+  float* lse2;
+  float* dsum;
   int BH;
   int N;
   int d;
@@ -80,6 +84,8 @@ cudaError_t launch_fwd_f32_tc(const FwdParams& p, void* workspace, EncodeTiledFn
 cudaError_t launch_fwd_keymajor(const FwdParams& p, const FwdMaps& m, void* workspace, cudaStream_t s);
 size_t keymajor_workspace_layout(int BH, int N, int d, size_t* off_m, size_t* off_l);
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
+// The main kernel of the d = 64 backward (one CTA per 128-key tile; grid = key tiles x B*H).
+cudaError_t launch_bwd_main_d64(const BwdParams& p, const BwdMaps& m, unsigned grid, cudaStream_t s);
 cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
 // Byte size of the backward workspace and the offsets of its lse2 / dsum
 // sections (dq_acc is at offset 0); rows are padded to multiples of 128.

@@ -82,10 +82,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Size in bytes of the workspace fa_bwd needs for a problem of this shape:
- * a float32 [B,H,N,d] dQ accumulator, then two float32 [B,H,Npad] arrays
- * (lse_i * log2(e) and D_i = sum_k dO_ik O_ik; Npad = N rounded up to a
- * multiple of 128), each section 256-byte aligned.  Returns 0 for
- * non-positive sizes.
+ * a float32 [B,H,N,d] dQ accumulator, then two [B,H,Npad] arrays derived
+ * from lse_i and from D_i = sum_k dO_ik O_ik (Npad = N rounded up to a
+ * multiple of 128; 4 bytes per row, or 16 bytes per row at d = 64, where
+ * each value is kept as three bf16 terms), each section 256-byte aligned.
+ * Returns 0 for non-positive sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 

@@ -50,6 +50,8 @@ def test_workspace_size(b):
     # dQ accumulator (15 floats -> 256 B), lse2 and D (128 padded rows each -> 512 B)
     assert b.fa_bwd_workspace_bytes(1, 1, 3, 5) == 256 + 512 + 512
     assert b.fa_bwd_workspace_bytes(2, 1, 129, 128) == 2 * 129 * 128 * 4 + 2 * (2 * 256 * 4)
+    # d = 64: 16 bytes per padded row in the two row arrays
+    assert b.fa_bwd_workspace_bytes(2, 1, 129, 64) == 2 * 129 * 64 * 4 + 2 * (2 * 256 * 16)
 
 
 def test_wait_limit_roundtrip(b):
