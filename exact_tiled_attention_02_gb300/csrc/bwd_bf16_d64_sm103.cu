@@ -86,9 +86,8 @@ constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
 constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr int OFF_OST = OFF_DST + DST_BYTES;
 constexpr int OFF_BAR = OFF_OST + 2 * OST_BOX;
-// kv_full, qa_full[3], qo_full[3], stage_free[3], s_full, dp_full, p_full, ds_full, dq_full, dq_free,
-// staged, ost_free, fin, drain
-constexpr int NBAR = 1 + 3 * STAGES + 10;
+// kv_full, st_full[3], stage_free[3], s_full, dp_full, p_full, ds_full, dq_full, staged, ost_free, fin, drain
+constexpr int NBAR = 1 + 2 * STAGES + 9;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 // the whole 227 KB: every address an MMA operand descriptor can form (16
@@ -102,23 +101,41 @@ static_assert(OFF_K % 1024 == 0 && OFF_STAGE % 1024 == 0 && OFF_DST % 1024 == 0 
 struct Bars {
   uint32_t base;
   __device__ uint32_t kv_full() const { return base; }
-  __device__ uint32_t qa_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t qo_full(int s) const { return base + 8 * (1 + STAGES + s); }
-  __device__ uint32_t stage_free(int s) const { return base + 8 * (1 + 2 * STAGES + s); }
-  __device__ uint32_t at(int k) const { return base + 8 * (1 + 3 * STAGES + k); }
+  __device__ uint32_t st_full(int s) const { return base + 8 * (1 + s); }  // Q_i, dO_i and their terms
+  __device__ uint32_t stage_free(int s) const { return base + 8 * (1 + STAGES + s); }
+  __device__ uint32_t at(int k) const { return base + 8 * (1 + 2 * STAGES + k); }
   __device__ uint32_t s_full() const { return at(0); }
   __device__ uint32_t dp_full() const { return at(1); }
   __device__ uint32_t p_full() const { return at(2); }
   __device__ uint32_t ds_full() const { return at(3); }
   __device__ uint32_t dq_full() const { return at(4); }
-  __device__ uint32_t dq_free() const { return at(5); }
-  __device__ uint32_t staged() const { return at(6); }
-  __device__ uint32_t ost_free() const { return at(7); }
-  __device__ uint32_t fin() const { return at(8); }
-  __device__ uint32_t drain() const { return at(9); }
+  __device__ uint32_t staged() const { return at(5); }
+  __device__ uint32_t ost_free() const { return at(6); }
+  __device__ uint32_t fin() const { return at(7); }
+  __device__ uint32_t drain() const { return at(8); }
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
+
+// Waits for two barrier phases.  Measured on the MMA thread: every wait whose
+// result gates the next tcgen05.mma leaves the tensor pipe idle for ~250
+// cycles even when the phase has long completed, so the common case (both
+// complete) tests both in one round trip.
+__device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, const WaitCtl& w) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+      "and.pred p, p, q;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0 || (mbar_wait(b1, p1, w) && mbar_wait(b2, p2, w));
+}
 
 // Shared-memory descriptor of a K-major operand without swizzle: 8-row groups
 // of 16-byte rows `sbo` bytes apart, the core matrix of the next 8 K-elements
@@ -168,8 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar.kv_full(), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar.qa_full(s), 1);
-      mbar_init(bar.qo_full(s), 1);
+      mbar_init(bar.st_full(s), 1);
       mbar_init(bar.stage_free(s), 1);  // tcgen05.commit after dK_i, the stage's last reader
     }
     mbar_init(bar.s_full(), 1);
@@ -177,7 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.p_full(), 8);  // one arrive per compute warp
     mbar_init(bar.ds_full(), 8);
     mbar_init(bar.dq_full(), 1);
-    mbar_init(bar.dq_free(), 8);
     mbar_init(bar.staged(), 8);
     mbar_init(bar.ost_free(), 1);  // the producer, once a reduction has read the staging tile
     mbar_init(bar.fin(), 1);
@@ -224,13 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = (t_lo + it) * BM;
         const uint32_t base = sStage + st * STAGE_BYTES;
         const uint32_t aug = sAug + st * 2 * AUG_BYTES;
-        mbar_arrive_expect_tx(bar.qa_full(st), TILE_BYTES + AUG_BYTES);
-        tma_load_3d(base, &tmq, bar.qa_full(st), 0, q0, bh);
+        mbar_arrive_expect_tx(bar.st_full(st), 2 * TILE_BYTES + 2 * AUG_BYTES);
+        tma_load_3d(base, &tmq, bar.st_full(st), 0, q0, bh);
         const size_t vrow = static_cast<size_t>(bh) * np + q0;
-        bulk_load(aug, reinterpret_cast<const uint8_t*>(p.lse2) + vrow * 16, AUG_BYTES, bar.qa_full(st));
-        mbar_arrive_expect_tx(bar.qo_full(st), TILE_BYTES + AUG_BYTES);
-        bulk_load(aug + AUG_BYTES, reinterpret_cast<const uint8_t*>(p.dsum) + vrow * 16, AUG_BYTES, bar.qo_full(st));
-        tma_load_3d(base + TILE_BYTES, &tmdo, bar.qo_full(st), 0, q0, bh);
+        bulk_load(aug, reinterpret_cast<const uint8_t*>(p.lse2) + vrow * 16, AUG_BYTES, bar.st_full(st));
+        bulk_load(aug + AUG_BYTES, reinterpret_cast<const uint8_t*>(p.dsum) + vrow * 16, AUG_BYTES, bar.st_full(st));
+        tma_load_3d(base + TILE_BYTES, &tmdo, bar.st_full(st), 0, q0, bh);
       };
       int loaded = 0;
       for (; loaded < STAGES && loaded < nsteps; ++loaded) load(loaded);
@@ -255,8 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         WaitCtl drain{nullptr, nullptr, wc.limit_ns};
         mbar_wait(bar.kv_full(), 0, drain);
         for (int it = max(0, loaded - STAGES); it < loaded; ++it) {
-          mbar_wait(bar.qa_full(it % STAGES), (it / STAGES) & 1, drain);
-          mbar_wait(bar.qo_full(it % STAGES), (it / STAGES) & 1, drain);
+          mbar_wait(bar.st_full(it % STAGES), (it / STAGES) & 1, drain);
         }
       }
     }
@@ -269,10 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_mm = idesc_bf16_f32(128, D, 1, 1);    // both MN-major (dS, K), N = 64
       // P^T / dS^T of query columns 16kk.. sit at TMEM column 8kk, or 64 + 8(kk - 4)
       auto pcol = [](int kk) { return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); };
-      auto issue_s = [&](int i) -> bool {  // S^T_i = K Q_i^T
+      // S^T_i = K Q_i^T (stage i % STAGES resident)
+      auto issue_s = [&](int i) {
         const int st = i % STAGES;
-        if (!mbar_wait(bar.qa_full(st), (i / STAGES) & 1, wc)) return false;
-        tc_fence_after();
         const uint32_t qb = sStage + st * STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -281,12 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qa = sAug + st * 2 * AUG_BYTES;  // + (1, 1, 1) . (-lse_q / scale terms)
         mma_bf16_ss(tmem + TM_S, sdesc_noswz(sOnes, sZero - sOnes, 128), sdesc_noswz(qa, sZero - qa, 128), id_kk, 1);
         mma_commit(bar.s_full());
-        return true;
       };
-      auto issue_dp = [&](int i) -> bool {  // dP^T_i = V dO_i^T
+      // dP^T_i = V dO_i^T (stage i % STAGES resident)
+      auto issue_dp = [&](int i) {
         const int st = i % STAGES;
-        if (!mbar_wait(bar.qo_full(st), (i / STAGES) & 1, wc)) return false;
-        tc_fence_after();
         const uint32_t ob = sStage + st * STAGE_BYTES + TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -295,25 +305,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t oa = sAug + st * 2 * AUG_BYTES + AUG_BYTES;  // + (1, 1, 1) . (-D_q terms)
         mma_bf16_ss(tmem + TM_DP, sdesc_noswz(sOnes, sZero - sOnes, 128), sdesc_noswz(oa, sZero - oa, 128), id_kk, 1);
         mma_commit(bar.dp_full());
-        return true;
       };
-      bool ok = mbar_wait(bar.kv_full(), 0, wc) && issue_s(0) && issue_dp(0);
+      bool ok = mbar_wait2(bar.kv_full(), 0, bar.st_full(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int i = 0; ok && i < nsteps; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = i & 1;
         const uint32_t qb = sStage + st * STAGE_BYTES;
-        // dV += P^T dO_i, then the next S^T into the columns P^T_i leaves
-        if (!mbar_wait(bar.p_full(), ph, wc)) break;
+        const bool more = i + 1 < nsteps;
+        // dV += P^T dO_i, then the next S^T into the columns P^T_i leaves (P_i
+        // in TMEM and, with it, stage i + 1 resident)
+        if (more ? !mbar_wait2(bar.p_full(), ph, bar.st_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)
+                 : !mbar_wait(bar.p_full(), ph, wc))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol(kk), sdesc_sw128(qb + TILE_BYTES + kk * 2048, TILE_BYTES, 1024),
                       id_kb, (i > 0 || kk > 0));
-        if (i + 1 < nsteps && !issue_s(i + 1)) break;
-        // dQ_i = dS K into its own columns (dQ_{i-1} has long been read out),
-        // first, so that it is ready when the warpgroups finish the next P
+        if (more) issue_s(i + 1);
+        // dQ_i = dS K into its own columns, first, so that it is ready when the
+        // warpgroups finish the next P.  (They read dQ_{i-1} out before
+        // computing dS_i: ds_full also frees the columns.)
         if (!mbar_wait(bar.ds_full(), ph, wc)) break;
-        if (i > 0 && !mbar_wait(bar.dq_free(), (i - 1) & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
@@ -327,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + TM_DK, tmem + TM_DP + pcol(kk), sdesc_sw128(qb + kk * 2048, TILE_BYTES, 1024), id_kb,
                       (i > 0 || kk > 0));
         mma_commit(bar.stage_free(st));
-        if (i + 1 < nsteps && !issue_dp(i + 1)) break;
+        if (more) issue_dp(i + 1);
       }
       mma_commit(bar.fin());
       mma_commit(bar.drain());
@@ -452,7 +470,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.dq_free());
       if (i > 0 && !warp_wait(bar.ost_free(), (i - 1) & 1)) {  // the previous reduction has read the tile
         ok = false;
         break;
