@@ -117,25 +117,6 @@ struct Bars {
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
 
-// Waits for two barrier phases.  Measured on the MMA thread: every wait whose
-// result gates the next tcgen05.mma leaves the tensor pipe idle for ~250
-// cycles even when the phase has long completed, so the common case (both
-// complete) tests both in one round trip.
-__device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, const WaitCtl& w) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred p, q;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n"
-      "and.pred p, p, q;\n"
-      "selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
-      : "memory");
-  return ok != 0 || (mbar_wait(b1, p1, w) && mbar_wait(b2, p2, w));
-}
 
 // Shared-memory descriptor of a K-major operand without swizzle: 8-row groups
 // of 16-byte rows `sbo` bytes apart, the core matrix of the next 8 K-elements

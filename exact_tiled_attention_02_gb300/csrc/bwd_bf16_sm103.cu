@@ -398,12 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       constexpr uint32_t id_kb = idesc_bf16_f32(128, C::DP, 0, 1);  // A K-major (TMEM), B MN-major, N = DP
       constexpr uint32_t id_mm = idesc_bf16_f32(128, C::DP, 1, 1);  // both MN-major (dS^T, K), N = DP
-      // S^T_i = K Q_i^T, then dP^T_i = V dO_i^T, each once its operand tile is resident
+      // S^T_i = K Q_i^T (the caller has waited for Q_i), then dP^T_i = V dO_i^T
+      // once dO_i is resident (the producer refills that half of the stage last)
       auto issue_s_dp = [&](int i) -> bool {
         const int st = i % STAGES;
         const uint32_t qb = sStage + st * STAGE_BYTES;
-        if (!mbar_wait(bar.qa_full(st), (i / STAGES) & 1, wc)) return false;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
@@ -421,7 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar.dp_full());
         return true;
       };
-      bool ok = mbar_wait(bar.kv_full(), 0, wc) && issue_s_dp(0);
+      bool ok = mbar_wait2(bar.kv_full(), 0, bar.qa_full(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s_dp(0);
+      }
       for (int i = 0; ok && i < nsteps; ++i) {
         const int st = i % STAGES;
         const uint32_t ph = i & 1;
@@ -449,8 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(qb + kk * 2048, BOX_BYTES, 1024), id_kb, (i > 0 || kk > 0));
         mma_commit(bar.dk_done());  // Q_i's last reader: its stage may take the dQ staging
         // next tile's S^T and dP^T once dQ has been read out of the S^T columns
+        // (and Q_{i+1} is resident: one round trip, see mbar_wait2)
         if (i + 1 < nsteps) {
-          if (!mbar_wait(bar.dq_free(), ph, wc)) break;
+          if (!mbar_wait2(bar.dq_free(), ph, bar.qa_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)) break;
+          tc_fence_after();
           if (!issue_s_dp(i + 1)) break;
         }
       }

@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++nq) {
         const Item w = decode_item<WIN>(item, N, r);
-        ok = mbar_wait(bar.q_full(0), nq & 1, wc) && mbar_wait(bar.q_full(1), nq & 1, wc);
+        ok = mbar_wait2(bar.q_full(0), nq & 1, bar.q_full(1), nq & 1, wc);
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t) {
@@ -366,18 +366,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int g = g0 + it;
             const int st = g % C::STAGES;
             const bool more = it + 1 < w.ntiles;
-            if (!mbar_wait(bar.v_full(st), (g / C::STAGES) & 1, wc) || !mbar_wait(bar.p_full(0), (cnt[0] + it) & 1, wc)) {
+            // V_j and P0_j in one round trip (see mbar_wait2); with a three-deep
+            // ring the next K is resident by then too (measured: +3% at d = 64),
+            // with two it may still be in flight (-5% at d = 128 when waited
+            // for here), so it gets its own wait after P0 V_j
+            const uint32_t pv = (g / C::STAGES) & 1, pp = (cnt[0] + it) & 1;
+            constexpr bool k_early = C::STAGES >= 3;
+            if (k_early && more ? !mbar_wait3(bar.v_full(st), pv, bar.p_full(0), pp, bar.k_full((g + 1) % C::STAGES),
+                                              ((g + 1) / C::STAGES) & 1, wc)
+                                : !mbar_wait2(bar.v_full(st), pv, bar.p_full(0), pp, wc)) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_pv(0, it, it == 0);
             if (more) {
-              if (!wait_k(it + 1)) {
-                ok = false;
-                break;
+              if (!k_early) {
+                if (!wait_k(it + 1)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
               }
-              tc_fence_after();
               issue_s(0, it + 1);
             }
             if (!mbar_wait(bar.p_full(1), (cnt[1] + it) & 1, wc)) {

@@ -172,6 +172,45 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
   }
 }
 
+// Waits for two or three barrier phases.  On a thread that issues tcgen05.mma,
+// every wait whose result gates the next MMA leaves the tensor pipe idle for
+// ~250 cycles even when the phase has long completed (measured: a satisfied
+// try_wait, a test_wait or a plain shared-memory load cost the same), so the
+// common case (all complete) tests them in one round trip.
+__device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, const WaitCtl& w) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+      "and.pred p, p, q;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0 || (mbar_wait(b1, p1, w) && mbar_wait(b2, p2, w));
+}
+__device__ __forceinline__ bool mbar_wait3(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, uint32_t b3,
+                                           uint32_t p3, const WaitCtl& w) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q, r;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 r, [%5], %6;\n"
+      "and.pred p, p, q;\n"
+      "and.pred p, p, r;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(b1), "r"(p1), "r"(b2), "r"(p2), "r"(b3), "r"(p3)
+      : "memory");
+  return ok != 0 || (mbar_wait(b1, p1, w) && mbar_wait(b2, p2, w) && mbar_wait(b3, p3, w));
+}
+
 // ---------------------------------------------------------------------------
 // TMA (no multicast): 3-D tiled tensor load into shared memory, completion
 // counted in bytes on an mbarrier.
