@@ -363,7 +363,8 @@ def main():
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     kname = {"fwd": "fwd_keymajor_sm103" if key_major else "fwd_f32_tc_sm103" if tf32x3 else
              "fwd_f32_simt" if w.dtype == "f32" else "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103",
-             "bwd": "bwd_f32_simt" if w.dtype == "f32" else "bwd_bf16_sm103"}[dom]
+             "bwd": "bwd_f32_simt" if w.dtype == "f32" else "bwd_bf16_d64_sm103" if w.d == 64 else
+             "bwd_bf16_sm103"}[dom]
     traffic = ncu_traffic(f"{kname}_{w.name}.md", kname + ".cu")
     roofline = {"bound": bound, "kernel": dom, "achieved": round(kernels[dom]["tflops"], 2),
                 "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
