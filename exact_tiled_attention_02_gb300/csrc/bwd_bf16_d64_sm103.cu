@@ -32,8 +32,8 @@
 // dK take 64 columns each and dQ gets 64 columns of its own:
 //   [0,128) S^T / P^T   [128,256) dP^T / dS^T   [256,320) dV   [320,384) dK
 //   [384,448) dQ
-// so the MMA warp issues, per step i,
-//   dV_i (once P_i is in TMEM), S^T_{i+1},
+// so, per step i, the MMA threads issue
+//   dV_i (once P_i is in TMEM), S^T_{i+1}, and, on the other thread,
 //   dQ_i (once dS_i is in shared memory), dK_i (once it is in TMEM), dP^T_{i+1}
 // and the compute warpgroups run dS_i, then P_{i+1} (its S^T_{i+1} already
 // computed), then the read-out of dQ_i: the exponentials of the next tile
@@ -46,8 +46,10 @@
 // Warp roles (384 threads): warps 0-3 and 4-7 are the two compute
 // warpgroups (query columns 0-63 / 64-127 of every tile; thread t owns key
 // row t == TMEM lane t, and for the dQ read-out query row t, warpgroup g
-// taking d columns [32g, 32g + 32)); warp 8 owns TMEM and issues the MMAs;
-// warp 9 is the TMA producer (loads, dQ reductions); warps 10-11 idle.
+// taking d columns [32g, 32g + 32)); warp 8 owns TMEM and issues dV and S^T;
+// warp 10 issues dQ, dK and dP^T (measured: 2.6% faster at 2x16x8192x64
+// than one issuing thread, whose sub-partition it shares with two compute
+// warps); warp 9 is the TMA producer (loads, dQ reductions); warp 11 idles.
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -86,8 +88,9 @@ constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
 constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr int OFF_OST = OFF_DST + DST_BYTES;
 constexpr int OFF_BAR = OFF_OST + 2 * OST_BOX;
-// kv_full, st_full[3], stage_free[3], s_full, dp_full, p_full, ds_full, dq_full, staged, ost_free, fin, drain
-constexpr int NBAR = 1 + 2 * STAGES + 9;
+// kv_full, st_full[3], stage_free[3], s_full, dp_full, p_full, ds_full, dq_full, staged, ost_free, fin, drain,
+// drain2
+constexpr int NBAR = 1 + 2 * STAGES + 10;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 // the whole 227 KB: every address an MMA operand descriptor can form (16
@@ -113,6 +116,7 @@ struct Bars {
   __device__ uint32_t ost_free() const { return at(6); }
   __device__ uint32_t fin() const { return at(7); }
   __device__ uint32_t drain() const { return at(8); }
+  __device__ uint32_t drain2() const { return at(9); }
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.kv_full(), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar.st_full(s), 1);
-      mbar_init(bar.stage_free(s), 1);  // tcgen05.commit after dK_i, the stage's last reader
+      mbar_init(bar.stage_free(s), 2);  // commits after dV_i and after dK_i, the stage's last readers
     }
     mbar_init(bar.s_full(), 1);
     mbar_init(bar.dp_full(), 1);
@@ -176,8 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.dq_full(), 1);
     mbar_init(bar.staged(), 8);
     mbar_init(bar.ost_free(), 1);  // the producer, once a reduction has read the staging tile
-    mbar_init(bar.fin(), 1);
+    mbar_init(bar.fin(), 2);  // one commit per MMA-issuing thread
     mbar_init(bar.drain(), 1);
+    mbar_init(bar.drain2(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc));
   };
 
-  if (warp >= 10) {
+  if (warp == 11) {
     // idle
   } else if (warp == 9) {
     // ------------------------------------------------------------ producer
@@ -255,83 +260,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 8) {
+  } else if (warp == 8 || warp == 10) {
     // ----------------------------------------------------------------- MMA
+    // Two issuing threads on two SM sub-partitions (each shares its
+    // sub-partition with two compute warps, whose instructions delay the
+    // issue): warp 8 issues dV_i and S^T_{i+1}, warp 10 dQ_i, dK_i and
+    // dP^T_{i+1}.  Neither writes what the other's products read, and each
+    // thread's products run in its issue order; the stage is free once both
+    // have committed (stage_free counts two).
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       constexpr uint32_t id_kb = idesc_bf16_f32(128, D, 0, 1);    // A from TMEM, B MN-major, N = 64
       constexpr uint32_t id_mm = idesc_bf16_f32(128, D, 1, 1);    // both MN-major (dS, K), N = 64
       // P^T / dS^T of query columns 16kk.. sit at TMEM column 8kk, or 64 + 8(kk - 4)
       auto pcol = [](int kk) { return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); };
-      // S^T_i = K Q_i^T (stage i % STAGES resident)
-      auto issue_s = [&](int i) {
-        const int st = i % STAGES;
-        const uint32_t qb = sStage + st * STAGE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + TM_S, sdesc_sw128(sK + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 32, 16, 1024), id_kk,
-                      kk > 0);
-        const uint32_t qa = sAug + st * 2 * AUG_BYTES;  // + (1, 1, 1) . (-lse_q / scale terms)
-        mma_bf16_ss(tmem + TM_S, sdesc_noswz(sOnes, sZero - sOnes, 128), sdesc_noswz(qa, sZero - qa, 128), id_kk, 1);
-        mma_commit(bar.s_full());
-      };
-      // dP^T_i = V dO_i^T (stage i % STAGES resident)
-      auto issue_dp = [&](int i) {
-        const int st = i % STAGES;
-        const uint32_t ob = sStage + st * STAGE_BYTES + TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + TM_DP, sdesc_sw128(sV + kk * 32, 16, 1024), sdesc_sw128(ob + kk * 32, 16, 1024), id_kk,
-                      kk > 0);
-        const uint32_t oa = sAug + st * 2 * AUG_BYTES + AUG_BYTES;  // + (1, 1, 1) . (-D_q terms)
-        mma_bf16_ss(tmem + TM_DP, sdesc_noswz(sOnes, sZero - sOnes, 128), sdesc_noswz(oa, sZero - oa, 128), id_kk, 1);
-        mma_commit(bar.dp_full());
-      };
+      const bool first = warp == 8;
       bool ok = mbar_wait2(bar.kv_full(), 0, bar.st_full(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
+      if (ok) tc_fence_after();
+      if (first) {
+        // S^T_i = K Q_i^T (stage i % STAGES resident)
+        auto issue_s = [&](int i) {
+          const int st = i % STAGES;
+          const uint32_t qb = sStage + st * STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + TM_S, sdesc_sw128(sK + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 32, 16, 1024), id_kk,
+                        kk > 0);
+          const uint32_t qa = sAug + st * 2 * AUG_BYTES;  // + (1, 1, 1) . (-lse_q / scale terms)
+          mma_bf16_ss(tmem + TM_S, sdesc_noswz(sOnes, sZero - sOnes, 128), sdesc_noswz(qa, sZero - qa, 128), id_kk,
+                      1);
+          mma_commit(bar.s_full());
+        };
+        if (ok) issue_s(0);
+        for (int i = 0; ok && i < nsteps; ++i) {
+          const int st = i % STAGES;
+          const uint32_t ph = i & 1;
+          const uint32_t qb = sStage + st * STAGE_BYTES;
+          const bool more = i + 1 < nsteps;
+          // dV += P^T dO_i, then the next S^T into the columns P^T_i leaves (P_i
+          // in TMEM and, with it, stage i + 1 resident)
+          if (more ? !mbar_wait2(bar.p_full(), ph, bar.st_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)
+                   : !mbar_wait(bar.p_full(), ph, wc))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol(kk),
+                        sdesc_sw128(qb + TILE_BYTES + kk * 2048, TILE_BYTES, 1024), id_kb, (i > 0 || kk > 0));
+          mma_commit(bar.stage_free(st));  // dO_i's last reader
+          if (more) issue_s(i + 1);
+        }
+        mma_commit(bar.fin());
+        mma_commit(bar.drain());
+        WaitCtl drain{nullptr, nullptr, wc.limit_ns};
+        mbar_wait(bar.drain(), 0, drain);
+      } else {
+        // dP^T_i = V dO_i^T (stage i % STAGES resident)
+        auto issue_dp = [&](int i) {
+          const int st = i % STAGES;
+          const uint32_t ob = sStage + st * STAGE_BYTES + TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + TM_DP, sdesc_sw128(sV + kk * 32, 16, 1024), sdesc_sw128(ob + kk * 32, 16, 1024), id_kk,
+                        kk > 0);
+          const uint32_t oa = sAug + st * 2 * AUG_BYTES + AUG_BYTES;  // + (1, 1, 1) . (-D_q terms)
+          mma_bf16_ss(tmem + TM_DP, sdesc_noswz(sOnes, sZero - sOnes, 128), sdesc_noswz(oa, sZero - oa, 128), id_kk,
+                      1);
+          mma_commit(bar.dp_full());
+        };
+        if (ok) issue_dp(0);
+        for (int i = 0; ok && i < nsteps; ++i) {
+          const int st = i % STAGES;
+          const uint32_t ph = i & 1;
+          const uint32_t qb = sStage + st * STAGE_BYTES;
+          const bool more = i + 1 < nsteps;
+          // dQ_i = dS K into its own columns, first, so that it is ready when the
+          // warpgroups finish the next P.  (They read dQ_{i-1} out before
+          // computing dS_i: ds_full also frees the columns.)
+          if (more ? !mbar_wait2(bar.ds_full(), ph, bar.st_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)
+                   : !mbar_wait(bar.ds_full(), ph, wc))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ss(tmem + TM_DQ, sdesc_sw128(sDS + kk * 2048, DST_BOX, 1024),
+                        sdesc_sw128(sK + kk * 2048, TILE_BYTES, 1024), id_mm, kk > 0);
+          mma_commit(bar.dq_full());
+          // dK += dS^T Q_i (Q_i's last reader), then the next dP^T into the
+          // columns dS^T_i leaves
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_bf16_ts(tmem + TM_DK, tmem + TM_DP + pcol(kk), sdesc_sw128(qb + kk * 2048, TILE_BYTES, 1024), id_kb,
+                        (i > 0 || kk > 0));
+          mma_commit(bar.stage_free(st));
+          if (more) issue_dp(i + 1);
+        }
+        mma_commit(bar.fin());
+        mma_commit(bar.drain2());
+        WaitCtl drain{nullptr, nullptr, wc.limit_ns};
+        mbar_wait(bar.drain2(), 0, drain);
       }
-      for (int i = 0; ok && i < nsteps; ++i) {
-        const int st = i % STAGES;
-        const uint32_t ph = i & 1;
-        const uint32_t qb = sStage + st * STAGE_BYTES;
-        const bool more = i + 1 < nsteps;
-        // dV += P^T dO_i, then the next S^T into the columns P^T_i leaves (P_i
-        // in TMEM and, with it, stage i + 1 resident)
-        if (more ? !mbar_wait2(bar.p_full(), ph, bar.st_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)
-                 : !mbar_wait(bar.p_full(), ph, wc))
-          break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol(kk), sdesc_sw128(qb + TILE_BYTES + kk * 2048, TILE_BYTES, 1024),
-                      id_kb, (i > 0 || kk > 0));
-        if (more) issue_s(i + 1);
-        // dQ_i = dS K into its own columns, first, so that it is ready when the
-        // warpgroups finish the next P.  (They read dQ_{i-1} out before
-        // computing dS_i: ds_full also frees the columns.)
-        if (!mbar_wait(bar.ds_full(), ph, wc)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ss(tmem + TM_DQ, sdesc_sw128(sDS + kk * 2048, DST_BOX, 1024),
-                      sdesc_sw128(sK + kk * 2048, TILE_BYTES, 1024), id_mm, kk > 0);
-        mma_commit(bar.dq_full());
-        // dK += dS^T Q_i (Q_i's last reader: the stage may be refilled), then the
-        // next dP^T into the columns dS^T_i leaves
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_bf16_ts(tmem + TM_DK, tmem + TM_DP + pcol(kk), sdesc_sw128(qb + kk * 2048, TILE_BYTES, 1024), id_kb,
-                      (i > 0 || kk > 0));
-        mma_commit(bar.stage_free(st));
-        if (more) issue_dp(i + 1);
-      }
-      mma_commit(bar.fin());
-      mma_commit(bar.drain());
-      WaitCtl drain{nullptr, nullptr, wc.limit_ns};
-      mbar_wait(bar.drain(), 0, drain);
     }
     __syncwarp();
   } else {
