@@ -75,6 +75,10 @@ BWD_CASES = [
     (2, 2, 300, 64, 0, 8.0),
     (1, 1, 513, 64, 0, 1.0),
     (1, 2, 700, 64, 65, 1.0),
+    # d = 64 adds -lse/scale and -D in the tensor core as three bf16 terms:
+    # large logits (large lse) over many query tiles, with and without a band
+    (1, 1, 2048, 64, 0, 8.0),
+    (1, 1, 1500, 64, 257, 8.0),
     (1, 1, 1, 96, 0, 1.0),
     (1, 2, 200, 96, 0, 1.0),
     (1, 1, 513, 96, 0, 8.0),
@@ -150,6 +154,30 @@ def test_workload5_full_size_sampled_heads():
     for g in (dq, dk, dv):
         assert torch.isfinite(g.float()).all()
     rng = np.random.default_rng(5)
+    heads = [(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))]
+    for b, h in heads:
+        refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), w.scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
+            assert _rel(_np(g), r) <= 1e-2, (name, b, h, _rel(_np(g), r))
+    # sum over keys of dK vanishes; sum over keys of dV equals the sum over queries of dO
+    sk = dk.float().sum(dim=2)
+    assert float(sk.abs().max()) <= 2e-2 * float(dk.float().abs().sum(dim=2).max())
+    sv = dv.float().sum(dim=2)
+    sdo = do.to(dev).float().sum(dim=2)
+    assert float((sv - sdo).norm() / sdo.norm()) <= 1e-2
+
+
+def test_workload2_full_size_sampled_heads():
+    """Workload 2 (d = 64) at full size, launched as the bench launches it:
+    three whole heads against the oracle, plus identities of the exact
+    gradient over every head."""
+    dev = _dev()
+    w = configs.WORKLOADS[2]
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    dq, dk, dv = _run(q, k, v, do, w.scale, w.window, dev)
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g.float()).all()
+    rng = np.random.default_rng(2)
     heads = [(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))]
     for b, h in heads:
         refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), w.scale)
