@@ -80,16 +80,17 @@ constexpr int VEC_BYTES = BM * 4;         // 512 B of lse*log2e or of D
 constexpr int DQ_BOX_BYTES = BM * 32 * 4; // 16 KB: fp32 dQ staging box [128 queries][32 d], 128-byte swizzled
 constexpr int DST_BYTES = BN * BM * 2;    // 32 KB: bf16 dS^T [128 keys][128 queries] as two boxes
 
-// D = 64, 96 or 128.  Tiles in shared memory are DP = D rounded up to a
-// multiple of 64 columns wide (whole 128-byte swizzle atoms; for D = 96 the
+// D = 96 or 128 (d = 64 has its own main kernel).  Tiles in shared memory
+// are DP = 128 columns wide (whole 128-byte swizzle atoms; for D = 96 the
 // TMA zero-fills columns 96..127).  S^T and dP^T contract over the D real
 // columns; the three products with N = d (dV, dK, dQ) run with N = DP, since a
 // 128-byte-swizzled MN-major operand is laid out in 64-column atoms: the zero
 // columns only produce zero columns, which are never read.
 template <int D>
 struct Cfg {
+  static_assert(D == 96 || D == 128, "d = 64 runs bwd_bf16_d64_sm103.cu");
   static constexpr int DP = (D + 63) / 64 * 64;
-  static constexpr int STAGES = (DP == 128) ? 2 : 3;  // Q/dO/lse/D ring depth
+  static constexpr int STAGES = 2;                    // Q/dO/lse/D ring depth
   static constexpr int BOXES = DP / 64;               // 64-column boxes per row of a Q / K / V / dO tile
   static constexpr int TILE_BYTES = 128 * DP * 2;     // a bf16 [128 x DP] tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // Q_i then dO_i; also holds the fp32 [128 x D] dQ staging
