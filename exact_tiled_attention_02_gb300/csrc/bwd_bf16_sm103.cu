@@ -1,9 +1,9 @@
 // bwd_bf16_sm103.cu -- exact attention backward by recomputation for GB300
-// (sm_103a), bf16 in / fp32 accumulate, head dimension d = 64, 96 or 128.
-// The prep and dq kernels here serve all three; the main kernel here serves
-// d = 96 and 128, and d = 64 has its own (bwd_bf16_d64_sm103.cu), which
-// TMEM room at that size lets overlap one query tile's element-wise work
-// with the next tile's products.
+// (sm_103a), bf16 in / fp32 accumulate: the main kernel for head dimension
+// d = 96 and 128, and the launcher for every bf16 head dimension (d = 64 has
+// its own main kernel, bwd_bf16_d64_sm103.cu, which TMEM room at that size
+// lets overlap one query tile's element-wise work with the next tile's
+// products; the prep and dq kernels are in bwd_prep_sm103.cu).
 //
 // "Flash attention and efficient attention -- Hinglish notes", "Backward Pass:
 // Recomputation": the N x N matrices S and P are not stored by the forward and
@@ -13,13 +13,8 @@
 // none): dV = P^T dO, dP = dO V^T, dS = P o (dP - D) with
 // D_i = sum_j P_ij dP_ij = sum_k dO_ik O_ik, dQ = scale dS K, dK = scale dS^T Q.
 //
-// Three kernels:
-//   bwd_prep     -D_i = -rowsum(dO o O) and -lse_i * log2(e) into the workspace
-//                (rows padded to a multiple of 128: D = 0, lse = +inf, so padded
-//                query rows get P = 0), and the fp32 dQ accumulator zeroed.
-//                For d = 64 it writes -lse_i / scale and -D_i instead, each as
-//                three bf16 terms, the operand rows that kernel's tensor core
-//                adds into S^T and dP^T.
+// Three launches: bwd_prep (-D_i and -lse_i log2 e per query row, the dQ
+// accumulator zeroed), then
 //   bwd_main     one CTA per 128-key tile of one (batch, head): K_j, V_j stay
 //                in shared memory; the CTA walks the 128-row query tiles that
 //                can see its keys (only in-band tiles when windowed) and, per
@@ -35,8 +30,8 @@
 //                swizzled boxes of 32 columns) in the shared-memory stage its
 //                Q / dO tiles just vacated, and added to the fp32 accumulator
 //                by TMA reductions (cp.reduce.async.bulk.tensor .add.f32), so
-//                the memory system does the adds in whole lines.
-//   bwd_dq       dQ = bf16(scale * accumulator).
+//                the memory system does the adds in whole lines;
+// then bwd_dq (dQ = bf16(scale * accumulator)).
 // (Measured on GB300: tcgen05.mma with M = 128 and K = 16 takes 64 cycles at
 // N = 128 but 48 at N = 64, so 64-row query tiles would waste a third of the
 // tensor core on three of the five products.)
@@ -142,97 +137,6 @@ struct Bars {
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
-
-// ---------------------------------------------------------------------------
-// bwd_prep: one warp per (padded) query row
-// ---------------------------------------------------------------------------
-// Three bf16 terms whose sum is x to fp32 precision (each term takes what the
-// previous ones left; the differences are exact in fp32), with five zeros:
-// one 16-byte row of a K = 16 operand whose other 8 elements are zero.
-__device__ __forceinline__ uint4 bf16_split3_row(float x) {
-  const __nv_bfloat16 h1 = __float2bfloat16_rn(x);
-  const float r1 = x - __bfloat162float(h1);
-  const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
-  const __nv_bfloat16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
-  uint4 v;
-  v.x = static_cast<uint32_t>(__bfloat16_as_ushort(h1)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h2)) << 16);
-  v.y = static_cast<uint32_t>(__bfloat16_as_ushort(h3));
-  v.z = 0u;
-  v.w = 0u;
-  return v;
-}
-
-__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
-                                                         const __nv_bfloat16* __restrict__ dO,
-                                                         const float* __restrict__ lse, float* __restrict__ lse2,
-                                                         float* __restrict__ dsum, float* __restrict__ dq_acc, int BH,
-                                                         int N, int d, float inv_scale, int split) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int np = npad128(N);
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // padded row index
-  if (row >= static_cast<long long>(BH) * np) return;
-  const long long bh = row / np;
-  const int i = static_cast<int>(row % np);
-  if (i >= N) {
-    if (lane == 0) {
-      if (split) {
-        // -lse / scale far below any logit: the row's P underflows to 0
-        reinterpret_cast<uint4*>(lse2)[row] = bf16_split3_row(-1e30f);
-        reinterpret_cast<uint4*>(dsum)[row] = bf16_split3_row(0.f);
-      } else {
-        lse2[row] = -INFINITY;
-        dsum[row] = 0.f;
-      }
-    }
-    return;
-  }
-  const long long src = (bh * N + i) * d;
-  float acc = 0.f;
-  // each pass: lane l reads 4 consecutive bf16 (8 bytes) of O and dO at column 4l
-  for (int c = lane * 4; c < d; c += 128) {
-    const uint2 ov = *reinterpret_cast<const uint2*>(o + src + c);
-    const uint2 gv = *reinterpret_cast<const uint2*>(dO + src + c);
-    const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
-    const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float2 a = __bfloat1622float2(op[e]);
-      const float2 b = __bfloat1622float2(gp[e]);
-      acc = fmaf(a.x, b.x, acc);
-      acc = fmaf(a.y, b.y, acc);
-    }
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    if (split) {
-      reinterpret_cast<uint4*>(lse2)[row] = bf16_split3_row(-lse[bh * N + i] * inv_scale);
-      reinterpret_cast<uint4*>(dsum)[row] = bf16_split3_row(-acc);
-    } else {
-      dsum[row] = -acc;
-      lse2[row] = -lse[bh * N + i] * 1.4426950408889634f;
-    }
-  }
-  float4* z = reinterpret_cast<float4*>(dq_acc + src);
-  for (int c = lane; c < d / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// ---------------------------------------------------------------------------
-// bwd_dq: dQ = bf16(scale * acc), 8 elements per thread
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                       long long n8, float scale) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-  uint4 out;
-  out.x = pack_bf16x2(a.x * scale, a.y * scale);
-  out.y = pack_bf16x2(a.z * scale, a.w * scale);
-  out.z = pack_bf16x2(b.x * scale, b.y * scale);
-  out.w = pack_bf16x2(b.z * scale, b.w * scale);
-  reinterpret_cast<uint4*>(dq)[i] = out;
-}
 
 // ---------------------------------------------------------------------------
 // bwd_main
@@ -659,17 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum) {
-  const size_t rows = static_cast<size_t>(BH) * N;
-  const size_t prow = static_cast<size_t>(BH) * npad128(N);
-  const size_t acc = (rows * d * sizeof(float) + 255) & ~size_t(255);
-  // d = 64 stores each row's value as three bf16 terms in a 16-byte row
-  const size_t vec = (prow * (d == 64 ? 16 : sizeof(float)) + 255) & ~size_t(255);
-  if (off_lse2) *off_lse2 = acc;
-  if (off_dsum) *off_dsum = acc + vec;
-  return acc + 2 * vec;
-}
-
 namespace {
 
 template <int D>
@@ -689,26 +582,16 @@ cudaError_t launch_main(const BwdParams& p, const BwdMaps& m, unsigned grid, cud
 
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s) {
   if (p.d != 128 && p.d != 96 && p.d != 64) return cudaErrorNotSupported;
-  const long long np = npad128(p.N);
-  const long long prep_rows = static_cast<long long>(p.BH) * np;
-  const long long prep_blocks = (prep_rows + 7) / 8;
   const long long nkt = (p.N + BN - 1) / BN;
   const long long grid = nkt * p.BH;
-  const long long n8 = static_cast<long long>(p.BH) * p.N * p.d / 8;
-  if (prep_blocks > 0x7fffffffLL || grid > 0x7fffffffLL || (n8 + 255) / 256 > 0x7fffffffLL)
-    return cudaErrorInvalidConfiguration;
-  fa_bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dO), p.lse, p.lse2, p.dsum,
-      p.dq_acc, p.BH, p.N, p.d, 1.f / p.scale, p.d == 64);
-  cudaError_t e = cudaGetLastError();
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e = launch_bwd_prep(p, s);
   if (e != cudaSuccess) return e;
   e = p.d == 128  ? launch_main<128>(p, m, static_cast<unsigned>(grid), s)
       : p.d == 96 ? launch_main<96>(p, m, static_cast<unsigned>(grid), s)
                   : launch_bwd_main_d64(p, m, static_cast<unsigned>(grid), s);
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
-      p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8, p.scale);
-  return cudaGetLastError();
+  return launch_bwd_dq(p, s);
 }
 
 }  // namespace fa

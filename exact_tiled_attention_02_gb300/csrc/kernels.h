@@ -84,6 +84,10 @@ cudaError_t launch_fwd_f32_tc(const FwdParams& p, void* workspace, EncodeTiledFn
 cudaError_t launch_fwd_keymajor(const FwdParams& p, const FwdMaps& m, void* workspace, cudaStream_t s);
 size_t keymajor_workspace_layout(int BH, int N, int d, size_t* off_m, size_t* off_l);
 cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s);
+// The backward's prep kernel (row terms, dQ accumulator zeroed) and final dQ
+// cast (bwd_prep_sm103.cu), shared by every head dimension.
+cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t s);
 // The main kernel of the d = 64 backward (one CTA per 128-key tile; grid = key tiles x B*H).
 cudaError_t launch_bwd_main_d64(const BwdParams& p, const BwdMaps& m, unsigned grid, cudaStream_t s);
 cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
