@@ -191,6 +191,49 @@ def test_workload2_full_size_sampled_heads():
     assert float((sv - sdo).norm() / sdo.norm()) <= 1e-2
 
 
+def test_workload3_backward_full_size_heads():
+    """The bench's own backward (workload 3: N = 8192, d = 128, Q,K x8, so
+    large logits), launched as the bench launches it: two whole heads
+    against the oracle, plus finiteness everywhere."""
+    dev = _dev()
+    w = configs.WORKLOADS[3]
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    dq, dk, dv = _run(q, k, v, do, w.scale, w.window, dev)
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g.float()).all()
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        refs = oracle.dense_backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(do[b, h]), w.scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), refs):
+            assert _rel(_np(g), r) <= 1e-2, (name, b, h, _rel(_np(g), r))
+
+
+def test_workload4_backward_full_size_slices():
+    """Workload 4 (N = 16384, window 257) at full size.  With a band of radius
+    r, dQ of query i needs keys within r of i, and dK, dV of key j need the
+    rows within r of j, whose lse and D need keys within 2r of j; so the
+    oracle's gradients of a slice [s, e) of the sequence are exact for queries
+    in [s + r, e - r) and keys in [s + 2r, e - 2r) (no margin at the
+    sequence's own ends).  Three slices of two heads are checked."""
+    dev = _dev()
+    w = configs.WORKLOADS[4]
+    r = (w.window - 1) // 2
+    q, k, v, do = inputs.workload_inputs(w, with_do=True)
+    dq, dk, dv = _run(q, k, v, do, w.scale, w.window, dev)
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g.float()).all()
+    n = w.N
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        for s0, e0 in ((0, 1024), (n // 2 - 512, n // 2 + 512), (n - 1024, n)):
+            refs = oracle.dense_backward(_np(q[b, h, s0:e0]), _np(k[b, h, s0:e0]), _np(v[b, h, s0:e0]),
+                                         _np(do[b, h, s0:e0]), w.scale, w.window)
+            qa, qb = (s0 + r if s0 > 0 else s0), (e0 - r if e0 < n else e0)
+            ka, kb = (s0 + 2 * r if s0 > 0 else s0), (e0 - 2 * r if e0 < n else e0)
+            for name, g, ref, (a, z) in zip(("dq", "dk", "dv"), (dq, dk, dv), refs, ((qa, qb), (ka, kb), (ka, kb))):
+                got = _np(g[b, h, a:z])
+                want = ref[a - s0:z - s0]
+                assert _rel(got, want) <= 1e-2, (name, b, h, s0, _rel(got, want))
+
+
 def test_bwd_unsupported_requests():
     dev = _dev()
     fa = _fa()
