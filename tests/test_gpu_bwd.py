@@ -75,6 +75,8 @@ BWD_CASES = [
     (2, 2, 300, 64, 0, 8.0),
     (1, 1, 513, 64, 0, 1.0),
     (1, 2, 700, 64, 65, 1.0),
+    (1, 2, 300, 64, 1, 1.0),  # window 1: P = I, so dQ = dK = 0 and dV = dO
+    (1, 1, 129, 64, 3, 8.0),
     # d = 64 adds -lse/scale and -D in the tensor core as three bf16 terms:
     # large logits (large lse) over many query tiles, with and without a band
     (1, 1, 2048, 64, 0, 8.0),

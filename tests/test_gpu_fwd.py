@@ -82,6 +82,7 @@ BF16_CASES = [
     (1, 2, 300, 128, 3, 1.0),
     (1, 1, 700, 128, 65, 1.0),
     (1, 2, 1000, 64, 257, 1.0),
+    (1, 2, 300, 64, 1, 1.0),  # window 1: each query sees only its own key, O = V
     (1, 1, 640, 128, 257, 8.0),
     (1, 1, 257, 128, 513, 1.0),
     # more work items than SMs, so each CTA walks several items and the two
