@@ -10,14 +10,23 @@
 // dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
 // dV_j = sum_i P_ij dO_i.
 //
-// Three kernels, one warp per row each, no atomics (bitwise repeatable):
-//   prep    D_i into the workspace;
-//   dq      one warp per query row i: lane t recomputes P and dS for key
-//           (tile start + t) of a 32-key tile; each lane then accumulates
-//           dQ_i's dimensions t, t+32, t+64, t+96 over the tile's keys;
-//   dkdv    one warp per key row j, the mirror image over 32-query tiles.
-// With a window of radius r, row i visits only keys |i - j| <= r and key j
-// only such queries, which is exactly where P is non-zero.
+// Three kernels, no atomics (bitwise repeatable):
+//   prep    D_i into the workspace, one warp per row;
+//   dkdv    one CTA of 256 threads per 64 keys of one head, over the 64-row
+//           query tiles that can see them: S^T and dP^T as 4 x 4 register
+//           blocks (thread (ty, tx): keys 4ty.., queries 4tx..), P^T and dS^T
+//           through shared memory, then dV and dK for keys 4ty.. and head
+//           columns tx, tx + 16, ... (eight per thread);
+//   dq      the mirror image: one CTA per 64 queries over the key tiles,
+//           S and dP as 4 x 4 blocks (queries 4ty.., keys 4tx..), dS through
+//           shared memory, dQ for queries 4ty.. and columns tx, tx + 16, ...
+// The streamed operand tiles sit in shared memory transposed ([d][64]), so
+// that four rows of one column are one 16-byte load; the tiles that are also
+// read one column at a time have 68-float rows, which spreads those loads
+// over the banks (at most two threads of a half-warp share one).  Head
+// dimensions that are not a multiple of 4 are padded with zeros.  With a
+// window of radius r each tile loop visits only the tiles in the band, and
+// the masked pairs get P = 0.
 #include <cmath>
 
 #include "kernels.h"
@@ -25,9 +34,11 @@
 namespace fa {
 namespace {
 
-constexpr int kWarpsPerBlock = 4;
+constexpr int kPrepWarps = 4;
+constexpr int T = 64;          // rows per tile (keys or queries)
+constexpr int kThreads = 256;
 constexpr int kMaxD = 128;
-constexpr int kPerLane = kMaxD / 32;
+constexpr int LD = 68;         // row stride (floats) of the tiles also read column-wise
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -35,19 +46,11 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// dot(a, b) over d elements: a in shared memory (the warp's own row), b in
-// global memory (a different row per lane).
-__device__ __forceinline__ float dot_row(const float* a, const float* __restrict__ b, int d) {
-  float acc = 0.f;
-  for (int c = 0; c < d; ++c) acc = fmaf(a[c], b[c], acc);
-  return acc;
-}
-
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kPrepWarps * 32)
     fa_bwd_f32_prep_kernel(const float* __restrict__ o, const float* __restrict__ dO, float* __restrict__ dsum,
                            long long rows, int d) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
+  const long long row = static_cast<long long>(blockIdx.x) * kPrepWarps + warp;
   if (row >= rows) return;
   const float* orow = o + row * d;
   const float* grow = dO + row * d;
@@ -57,117 +60,237 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   if (lane == 0) dsum[row] = acc;
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    fa_bwd_f32_dq_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
-                         const float* __restrict__ lse, const float* __restrict__ dO,
-                         const float* __restrict__ dsum, float* __restrict__ dq, long long rows, int N, int d,
-                         int window_r, float scale) {
-  __shared__ float sq[kWarpsPerBlock][kMaxD];
-  __shared__ float sg[kWarpsPerBlock][kMaxD];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
-  if (row >= rows) return;  // whole warp leaves together
-  const long long bh = row / N;
-  const int i = static_cast<int>(row % N);
-  const float* kh = k + bh * static_cast<long long>(N) * d;
-  const float* vh = v + bh * static_cast<long long>(N) * d;
-  for (int c = lane; c < d; c += 32) {
-    sq[warp][c] = q[row * d + c];
-    sg[warp][c] = dO[row * d + c];
-  }
-  __syncwarp();
-  const float lse_i = lse[row], D_i = dsum[row];
-
-  int lo = 0, hi = N;
-  if (window_r >= 0) {
-    lo = max(0, i - window_r);
-    hi = min(N, i + window_r + 1);
-  }
-  float acc[kPerLane] = {0.f, 0.f, 0.f, 0.f};
-  for (int j0 = lo; j0 < hi; j0 += 32) {
-    const int j = j0 + lane;
-    float ds = 0.f;
-    if (j < hi) {
-      const float p = expf(dot_row(sq[warp], kh + static_cast<long long>(j) * d, d) * scale - lse_i);
-      const float dp = dot_row(sg[warp], vh + static_cast<long long>(j) * d, d);
-      ds = p * (dp - D_i);
+// rows [r0, r0 + 64) of a [N][d] matrix into shared memory transposed:
+// dst[c * ld + row] for c < dp (d rounded up to 4), zero past N and past d
+__device__ __forceinline__ void load_t(float* dst, int ld, const float* __restrict__ src, int r0, int N, int d,
+                                       int dp) {
+  const int tid = threadIdx.x;
+  if ((d & 3) == 0) {
+    for (int idx = tid; idx < T * (dp >> 2); idx += kThreads) {
+      const int row = idx & (T - 1), c4 = idx >> 6;  // consecutive threads, consecutive rows
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r0 + row < N) v = *reinterpret_cast<const float4*>(src + static_cast<long long>(r0 + row) * d + 4 * c4);
+      dst[(4 * c4 + 0) * ld + row] = v.x;
+      dst[(4 * c4 + 1) * ld + row] = v.y;
+      dst[(4 * c4 + 2) * ld + row] = v.z;
+      dst[(4 * c4 + 3) * ld + row] = v.w;
     }
-    const int cnt = min(32, hi - j0);
-    for (int jj = 0; jj < cnt; ++jj) {
-      const float db = __shfl_sync(0xffffffffu, ds, jj);
-      const float* kr = kh + static_cast<long long>(j0 + jj) * d;
-#pragma unroll
-      for (int t = 0; t < kPerLane; ++t) {
-        const int c = lane + 32 * t;
-        if (c < d) acc[t] = fmaf(db, kr[c], acc[t]);
-      }
+  } else {
+    for (int idx = tid; idx < T * dp; idx += kThreads) {
+      const int row = idx & (T - 1), c = idx >> 6;
+      dst[c * ld + row] = (r0 + row < N && c < d) ? src[static_cast<long long>(r0 + row) * d + c] : 0.f;
     }
-  }
-#pragma unroll
-  for (int t = 0; t < kPerLane; ++t) {
-    const int c = lane + 32 * t;
-    if (c < d) dq[row * d + c] = acc[t] * scale;
   }
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    fa_bwd_f32_dkdv_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
-                           const float* __restrict__ lse, const float* __restrict__ dO,
-                           const float* __restrict__ dsum, float* __restrict__ dk, float* __restrict__ dv,
-                           long long rows, int N, int d, int window_r, float scale) {
-  __shared__ float sk[kWarpsPerBlock][kMaxD];
-  __shared__ float sv[kWarpsPerBlock][kMaxD];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
-  if (row >= rows) return;
-  const long long bh = row / N;
-  const int j = static_cast<int>(row % N);
-  const long long head = bh * static_cast<long long>(N);
-  const float* qh = q + head * d;
-  const float* gh = dO + head * d;
-  for (int c = lane; c < d; c += 32) {
-    sk[warp][c] = k[row * d + c];
-    sv[warp][c] = v[row * d + c];
-  }
-  __syncwarp();
-
-  int lo = 0, hi = N;
-  if (window_r >= 0) {
-    lo = max(0, j - window_r);
-    hi = min(N, j + window_r + 1);
-  }
-  float acc_k[kPerLane] = {0.f, 0.f, 0.f, 0.f};
-  float acc_v[kPerLane] = {0.f, 0.f, 0.f, 0.f};
-  for (int i0 = lo; i0 < hi; i0 += 32) {
-    const int i = i0 + lane;
-    float p = 0.f, ds = 0.f;
-    if (i < hi) {
-      p = expf(dot_row(sk[warp], qh + static_cast<long long>(i) * d, d) * scale - lse[head + i]);
-      const float dp = dot_row(sv[warp], gh + static_cast<long long>(i) * d, d);
-      ds = p * (dp - dsum[head + i]);
-    }
-    const int cnt = min(32, hi - i0);
-    for (int ii = 0; ii < cnt; ++ii) {
-      const float pb = __shfl_sync(0xffffffffu, p, ii);
-      const float db = __shfl_sync(0xffffffffu, ds, ii);
-      const float* qr = qh + static_cast<long long>(i0 + ii) * d;
-      const float* gr = gh + static_cast<long long>(i0 + ii) * d;
+// 4 x 4 block of A B^T over c < dp: rows 4ty.. of A, rows 4tx.. of B, both
+// stored transposed (a[c * lda + row])
+__device__ __forceinline__ void block_abt(float (&acc)[4][4], const float* a, int lda, const float* b, int ldb, int dp,
+                                          int ty, int tx) {
 #pragma unroll
-      for (int t = 0; t < kPerLane; ++t) {
-        const int c = lane + 32 * t;
-        if (c < d) {
-          acc_v[t] = fmaf(pb, gr[c], acc_v[t]);
-          acc_k[t] = fmaf(db, qr[c], acc_k[t]);
-        }
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < dp; ++c) {
+    const float4 x = *reinterpret_cast<const float4*>(a + c * lda + 4 * ty);
+    const float4 y = *reinterpret_cast<const float4*>(b + c * ldb + 4 * tx);
+    const float xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], yv[j], acc[i][j]);
+  }
+}
+
+// acc[i][m] += sum_r w[(4ty + i) * T + r] * b[(tx + 16 m) * LD + r] over the
+// 64 rows r of a tile: w row-major [64][64], b transposed with LD-float rows
+__device__ __forceinline__ void accum_wb(float (&acc)[4][8], const float* w, const float* b, int ty, int tx, bool hi) {
+#pragma unroll 2
+  for (int r4 = 0; r4 < T; r4 += 4) {
+    float wv[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 t = *reinterpret_cast<const float4*>(w + (4 * ty + i) * T + r4);
+      wv[i][0] = t.x;
+      wv[i][1] = t.y;
+      wv[i][2] = t.z;
+      wv[i][3] = t.w;
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m >= 4 && !hi) break;
+        const float bv = b[(tx + 16 * m) * LD + r4 + rr];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][m] = fmaf(wv[i][rr], bv, acc[i][m]);
       }
     }
   }
+}
+
+// shared memory of both tile kernels, in floats
+constexpr int SMEM_FLOATS = 2 * kMaxD * T + 2 * kMaxD * LD + 2 * T * T;
+constexpr int SMEM_BYTES = SMEM_FLOATS * 4;
+
+// ---------------------------------------------------------------------------
+// dK, dV: one CTA per 64 keys
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_f32_dkdv_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+                           const float* __restrict__ lse, const float* __restrict__ dO,
+                           const float* __restrict__ dsum, float* __restrict__ dk, float* __restrict__ dv, int N,
+                           int d, int window_r, float scale) {
+  extern __shared__ float4 smem4[];
+  float* Kt = reinterpret_cast<float*>(smem4);  // [d][64]
+  float* Vt = Kt + kMaxD * T;                   // [d][64]
+  float* Qt = Vt + kMaxD * T;                   // [d][LD]
+  float* Gt = Qt + kMaxD * LD;                  // dO, [d][LD]
+  float* Ps = Gt + kMaxD * LD;                  // P^T [64 keys][64 queries]
+  float* Ss = Ps + T * T;                       // dS^T [64 keys][64 queries]
+  const int nkt = (N + T - 1) / T;
+  const long long bh = blockIdx.x / nkt;
+  const int k0 = (blockIdx.x % nkt) * T;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int dp = (d + 3) & ~3;
+  const bool hi = dp > 64;  // head columns 64.. exist
+  const long long head = bh * static_cast<long long>(N) * d;
+  load_t(Kt, T, k + head, k0, N, d, dp);
+  load_t(Vt, T, v + head, k0, N, d, dp);
+  int i_lo = 0, i_hi = N;  // queries that see some key of this tile
+  if (window_r >= 0) {
+    i_lo = max(0, k0 - window_r);
+    i_hi = min(N, k0 + T - 1 + window_r + 1);
+  }
+  float acc_k[4][8], acc_v[4][8];
 #pragma unroll
-  for (int t = 0; t < kPerLane; ++t) {
-    const int c = lane + 32 * t;
-    if (c < d) {
-      dk[row * d + c] = acc_k[t] * scale;
-      dv[row * d + c] = acc_v[t];
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      acc_k[i][m] = 0.f;
+      acc_v[i][m] = 0.f;
+    }
+  for (int q0 = (i_lo / T) * T; q0 < i_hi; q0 += T) {
+    __syncthreads();  // the previous tile's Q, dO, P^T, dS^T are no longer read
+    load_t(Qt, LD, q + head, q0, N, d, dp);
+    load_t(Gt, LD, dO + head, q0, N, d, dp);
+    __syncthreads();
+    float s[4][4], g[4][4];
+    block_abt(s, Kt, T, Qt, LD, dp, ty, tx);  // S^T: keys 4ty.., queries 4tx..
+    block_abt(g, Vt, T, Gt, LD, dp, ty, tx);  // dP^T
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int i = q0 + 4 * tx + jj;
+      const bool qok = i < N;
+      const float l_i = qok ? lse[bh * N + i] : 0.f, d_i = qok ? dsum[bh * N + i] : 0.f;
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const int j = k0 + 4 * ty + ii;
+        const bool in = qok && j < N && (window_r < 0 || (j >= i - window_r && j <= i + window_r));
+        const float pij = in ? expf(s[ii][jj] * scale - l_i) : 0.f;
+        s[ii][jj] = pij;
+        g[ii][jj] = pij * (g[ii][jj] - d_i);
+      }
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      *reinterpret_cast<float4*>(Ps + (4 * ty + ii) * T + 4 * tx) = make_float4(s[ii][0], s[ii][1], s[ii][2], s[ii][3]);
+      *reinterpret_cast<float4*>(Ss + (4 * ty + ii) * T + 4 * tx) = make_float4(g[ii][0], g[ii][1], g[ii][2], g[ii][3]);
+    }
+    __syncthreads();
+    accum_wb(acc_v, Ps, Gt, ty, tx, hi);  // dV += P^T dO
+    accum_wb(acc_k, Ss, Qt, ty, tx, hi);  // dK += dS^T Q
+  }
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int j = k0 + 4 * ty + ii;
+    if (j >= N) continue;
+    float* krow = dk + head + static_cast<long long>(j) * d;
+    float* vrow = dv + head + static_cast<long long>(j) * d;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int c = tx + 16 * m;
+      if (c < d) {
+        krow[c] = acc_k[ii][m] * scale;
+        vrow[c] = acc_v[ii][m];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per 64 queries
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_f32_dq_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+                         const float* __restrict__ lse, const float* __restrict__ dO,
+                         const float* __restrict__ dsum, float* __restrict__ dq, int N, int d, int window_r,
+                         float scale) {
+  extern __shared__ float4 smem4[];
+  float* Qt = reinterpret_cast<float*>(smem4);  // [d][64]
+  float* Gt = Qt + kMaxD * T;                   // dO, [d][64]
+  float* Kt = Gt + kMaxD * T;                   // [d][LD]
+  float* Vt = Kt + kMaxD * LD;                  // [d][LD]
+  float* Ss = Vt + kMaxD * LD;                  // dS [64 queries][64 keys]
+  const int nqt = (N + T - 1) / T;
+  const long long bh = blockIdx.x / nqt;
+  const int q0 = (blockIdx.x % nqt) * T;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int dp = (d + 3) & ~3;
+  const bool hi = dp > 64;
+  const long long head = bh * static_cast<long long>(N) * d;
+  load_t(Qt, T, q + head, q0, N, d, dp);
+  load_t(Gt, T, dO + head, q0, N, d, dp);
+  int j_lo = 0, j_hi = N;  // keys that some query of this tile sees
+  if (window_r >= 0) {
+    j_lo = max(0, q0 - window_r);
+    j_hi = min(N, q0 + T - 1 + window_r + 1);
+  }
+  float l_i[4], d_i[4];
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = q0 + 4 * ty + ii;
+    l_i[ii] = i < N ? lse[bh * N + i] : 0.f;
+    d_i[ii] = i < N ? dsum[bh * N + i] : 0.f;
+  }
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[i][m] = 0.f;
+  for (int k0 = (j_lo / T) * T; k0 < j_hi; k0 += T) {
+    __syncthreads();  // the previous tile's K, V, dS are no longer read
+    load_t(Kt, LD, k + head, k0, N, d, dp);
+    load_t(Vt, LD, v + head, k0, N, d, dp);
+    __syncthreads();
+    float s[4][4], g[4][4];
+    block_abt(s, Qt, T, Kt, LD, dp, ty, tx);  // S: queries 4ty.., keys 4tx..
+    block_abt(g, Gt, T, Vt, LD, dp, ty, tx);  // dP
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const int i = q0 + 4 * ty + ii;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = k0 + 4 * tx + jj;
+        const bool in = i < N && j < N && (window_r < 0 || (j >= i - window_r && j <= i + window_r));
+        const float pij = in ? expf(s[ii][jj] * scale - l_i[ii]) : 0.f;
+        g[ii][jj] = pij * (g[ii][jj] - d_i[ii]);
+      }
+      *reinterpret_cast<float4*>(Ss + (4 * ty + ii) * T + 4 * tx) = make_float4(g[ii][0], g[ii][1], g[ii][2], g[ii][3]);
+    }
+    __syncthreads();
+    accum_wb(acc, Ss, Kt, ty, tx, hi);  // dQ += dS K
+  }
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = q0 + 4 * ty + ii;
+    if (i >= N) continue;
+    float* qrow = dq + head + static_cast<long long>(i) * d;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int c = tx + 16 * m;
+      if (c < d) qrow[c] = acc[ii][m] * scale;
     }
   }
 }
@@ -175,26 +298,35 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 }  // namespace
 
 cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s) {
+  if (p.d > kMaxD || p.d < 1) return cudaErrorInvalidConfiguration;
   const long long rows = static_cast<long long>(p.BH) * p.N;
-  const long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  if (blocks > 0x7fffffffLL || p.d > kMaxD) return cudaErrorInvalidConfiguration;
-  const unsigned grid = static_cast<unsigned>(blocks);
+  const long long prep_blocks = (rows + kPrepWarps - 1) / kPrepWarps;
+  const long long tiles = static_cast<long long>(p.BH) * ((p.N + T - 1) / T);
+  if (prep_blocks > 0x7fffffffLL || tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_f32_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_bwd_f32_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   const float* q = static_cast<const float*>(p.q);
   const float* k = static_cast<const float*>(p.k);
   const float* v = static_cast<const float*>(p.v);
   const float* dO = static_cast<const float*>(p.dO);
   // D_i uses the workspace's D section as a plain [B*H*N] array
-  fa_bwd_f32_prep_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(static_cast<const float*>(p.o), dO, p.dsum, rows,
-                                                               p.d);
+  fa_bwd_f32_prep_kernel<<<static_cast<unsigned>(prep_blocks), kPrepWarps * 32, 0, s>>>(
+      static_cast<const float*>(p.o), dO, p.dsum, rows, p.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_f32_dq_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dq),
-                                                             rows, p.N, p.d, p.window_r, p.scale);
+  fa_bwd_f32_dq_kernel<<<static_cast<unsigned>(tiles), kThreads, SMEM_BYTES, s>>>(
+      q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dq), p.N, p.d, p.window_r, p.scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_f32_dkdv_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(q, k, v, p.lse, dO, p.dsum,
-                                                               static_cast<float*>(p.dk), static_cast<float*>(p.dv),
-                                                               rows, p.N, p.d, p.window_r, p.scale);
+  fa_bwd_f32_dkdv_kernel<<<static_cast<unsigned>(tiles), kThreads, SMEM_BYTES, s>>>(
+      q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dk), static_cast<float*>(p.dv), p.N, p.d, p.window_r,
+      p.scale);
   return cudaGetLastError();
 }
 
