@@ -263,6 +263,7 @@ F32_BWD_CASES = [
     # B, H, N, d, window
     (1, 1, 1, 4, 0), (1, 2, 5, 4, 0), (2, 1, 33, 17, 0), (1, 3, 100, 64, 0), (1, 1, 77, 128, 0),
     (1, 2, 50, 8, 3), (1, 1, 200, 32, 65), (2, 2, 129, 4, 257), (1, 1, 600, 128, 0),
+    (1, 1, 130, 65, 0), (1, 2, 300, 96, 0), (1, 1, 1000, 127, 129),
 ]
 
 

@@ -58,6 +58,10 @@ def test_workload1_f32_exact():
 @pytest.mark.parametrize("B,H,N,d,window", [
     (1, 1, 1, 1, 0), (1, 2, 5, 4, 0), (2, 1, 33, 17, 0), (1, 3, 100, 64, 0), (1, 1, 77, 128, 0),
     (1, 2, 50, 8, 3), (1, 1, 200, 32, 65), (2, 2, 129, 4, 257),
+    # head dimensions past 64 that are not a multiple of 4 (scalar tile loads,
+    # zero padding up to the next multiple of 4), d = 96, and a band that
+    # crosses several 64-row tiles
+    (1, 1, 130, 65, 0), (1, 2, 300, 96, 0), (1, 1, 1000, 127, 129),
 ])
 def test_f32_shapes(B, H, N, d, window):
     dev = _dev()
