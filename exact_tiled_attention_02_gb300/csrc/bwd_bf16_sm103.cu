@@ -169,8 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N, r = p.window_r;
   const int nkt = (N + BN - 1) / BN;
-  const int bh = blockIdx.x / nkt;
-  const int k0 = (blockIdx.x % nkt) * BN;
+  // CTAs past n_full take one half of a split key tile's query tiles each
+  int tile = static_cast<int>(blockIdx.x), half = -1;
+  if (tile >= p.n_full) {
+    half = (tile - p.n_full) & 1;
+    tile = p.n_full + ((tile - p.n_full) >> 1);
+  }
+  const int bh = tile / nkt;
+  const int k0 = (tile % nkt) * BN;
   const int np = npad128(N);
 
   // query tiles that can see this key tile
@@ -178,6 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (r >= 0) {
     t_lo = max(0, k0 - r) / BM;
     t_hi = (min(N, k0 + BN + r) + BM - 1) / BM;
+  }
+  if (half >= 0) {
+    const int mid = t_lo + (t_hi - t_lo) / 2;
+    if (half == 0)
+      t_hi = mid;
+    else
+      t_lo = mid;
   }
   const int nsteps = t_hi - t_lo;
 
@@ -518,7 +531,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1.3 us of a 77 us CTA at 4x16x4096x128)
     const bool have = ok && warp_wait(bar.fin(), 0);
     const uint32_t stage_out = g == 0 ? sK : sV;
-    if (have) {
+    if (have && half >= 0) {
+      // one half of a split key tile: add this row's fp32 values into the
+      // partial rows (both halves add into zeroed memory, so the sum does not
+      // depend on their order)
+      tc_fence_after();
+      const uint32_t tcol = g == 0 ? TM_DV : TM_DK;
+      const float mul = g == 0 ? 1.f : p.scale;
+      float* dst = p.kv_part + ((static_cast<size_t>(tile - p.n_full) * 2 + g) * BN + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tl + tcol + c * 32, v);
+        tmem_wait_ld();
+        if (k0 + row < N) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4_f32(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                           __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+        }
+      }
+    } else if (have) {
       tc_fence_after();
       const uint32_t tcol = g == 0 ? TM_DV : TM_DK;
       const float mul = g == 0 ? 1.f : p.scale;
@@ -541,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     named_bar_sync(1 + g, 128);
-    if (have && !*abort_flag) {
+    if (have && half < 0 && !*abort_flag) {
       uint8_t* gout = reinterpret_cast<uint8_t*>(g == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * N + k0) * D * 2;
       constexpr int CHUNKS = D / 8;
       for (int idx = row; idx < BN * CHUNKS; idx += 128) {
@@ -580,10 +613,34 @@ cudaError_t launch_main(const BwdParams& p, const BwdMaps& m, unsigned grid, cud
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16_tc(const BwdParams& p, const BwdMaps& m, cudaStream_t s) {
-  if (p.d != 128 && p.d != 96 && p.d != 64) return cudaErrorNotSupported;
+namespace {
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16_tc(const BwdParams& p_in, const BwdMaps& m, cudaStream_t s) {
+  if (p_in.d != 128 && p_in.d != 96 && p_in.d != 64) return cudaErrorNotSupported;
+  BwdParams p = p_in;
   const long long nkt = (p.N + BN - 1) / BN;
-  const long long grid = nkt * p.BH;
+  const long long tiles = nkt * p.BH;
+  // One CTA per SM.  When the last wave would hold at most half the SMs, its
+  // key tiles are split in two (d = 96, 128, no window, at least two query
+  // tiles): 2w half-length CTAs instead of w full ones.
+  long long split = 0;
+  if (p.d != 64 && p.window_r < 0 && p.N > BM) {
+    const int sms = device_sm_count();
+    const long long w = sms > 0 ? tiles % sms : 0;
+    if (w > 0 && 2 * w <= sms && w <= kMaxSplitTiles) split = w;
+  }
+  p.n_split = static_cast<int>(split);
+  p.n_full = static_cast<int>(tiles - split);
+  const long long grid = tiles + split;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = launch_bwd_prep(p, s);
   if (e != cudaSuccess) return e;

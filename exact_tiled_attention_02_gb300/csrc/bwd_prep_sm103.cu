@@ -12,8 +12,10 @@
 //             and -D_i as three bf16 terms each, the operand rows that kernel's
 //             tensor core adds in), and the row of the fp32 dQ accumulator
 //             zeroed.  Rows are padded to a multiple of 128: padding rows get
-//             D = 0 and a term that makes their P 0.
-//   bwd_dq    dQ = bf16(scale * accumulator).
+//             D = 0 and a term that makes their P 0.  Blocks past the rows
+//             zero the fp32 dV / dK partial rows of the split key tiles.
+//   bwd_dq    dQ = bf16(scale * accumulator); blocks past it convert the
+//             split key tiles' dV / dK partial sums to bf16.
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -47,7 +49,15 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ lse2,
                                                          float* __restrict__ dsum, float* __restrict__ dq_acc, int BH,
-                                                         int N, int d, float inv_scale, int split) {
+                                                         int N, int d, float inv_scale, int split,
+                                                         long long row_blocks, float* __restrict__ kv_part,
+                                                         long long part4) {
+  if (blockIdx.x >= row_blocks) {
+    // zero the split tiles' partial rows, one float4 per thread
+    const long long i = (static_cast<long long>(blockIdx.x) - row_blocks) * 256 + threadIdx.x;
+    if (i < part4) reinterpret_cast<float4*>(kv_part)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int np = npad128(N);
   const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // padded row index
@@ -97,11 +107,38 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   for (int c = lane; c < d / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = bf16(scale * acc), 8 elements per thread
+// dQ = bf16(scale * acc), 8 elements per thread; threads past the n8 groups
+// of dQ convert the split key tiles' partial rows (already scaled) into dV
+// and dK, 8 elements each
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                       long long n8, float scale) {
+                                                       long long n8, float scale, const float* __restrict__ kv_part,
+                                                       __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                                       int n_full, int n_split, int N, int d) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
+  if (i >= n8) {
+    const int c8n = d / 8;                          // 8-element groups per row
+    const long long per = 128LL * c8n;              // groups per (tile, dV or dK)
+    const long long u = i - n8;
+    if (u >= 2 * per * n_split) return;
+    const int s = static_cast<int>(u / (2 * per));  // split tile
+    const int which = static_cast<int>((u / per) & 1);
+    const int row = static_cast<int>((u % per) / c8n), c8 = static_cast<int>(u % c8n);
+    const int nkt = (N + 127) / 128;
+    const int tile = n_full + s;
+    const long long bh = tile / nkt;
+    const int kr = (tile % nkt) * 128 + row;
+    if (kr >= N) return;
+    const float4* src = reinterpret_cast<const float4*>(kv_part + u * 8);
+    const float4 a = src[0], b = src[1];
+    uint4 out;
+    out.x = pack_bf16x2(a.x, a.y);
+    out.y = pack_bf16x2(a.z, a.w);
+    out.z = pack_bf16x2(b.x, b.y);
+    out.w = pack_bf16x2(b.z, b.w);
+    __nv_bfloat16* dst = which == 0 ? dv : dk;
+    *reinterpret_cast<uint4*>(dst + (bh * N + kr) * d + 8 * c8) = out;
+    return;
+  }
   const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
   const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
   uint4 out;
@@ -114,32 +151,41 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
 
 }  // namespace
 
-size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum) {
+size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum, size_t* off_part) {
   const size_t rows = static_cast<size_t>(BH) * N;
   const size_t prow = static_cast<size_t>(BH) * npad128(N);
   const size_t acc = (rows * d * sizeof(float) + 255) & ~size_t(255);
   // d = 64 stores each row's value as three bf16 terms in a 16-byte row
   const size_t vec = (prow * (d == 64 ? 16 : sizeof(float)) + 255) & ~size_t(255);
+  // d = 96, 128: fp32 dV and dK rows of up to kMaxSplitTiles split key tiles
+  const size_t tiles = static_cast<size_t>(BH) * ((N + 127) / 128);
+  const size_t split = (d == 96 || d == 128) ? (tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles) : 0;
+  const size_t part = split * 2 * 128 * d * sizeof(float);  // a multiple of 256
   if (off_lse2) *off_lse2 = acc;
   if (off_dsum) *off_dsum = acc + vec;
-  return acc + 2 * vec;
+  if (off_part) *off_part = acc + 2 * vec;
+  return acc + 2 * vec + part;
 }
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t s) {
   const long long rows = static_cast<long long>(p.BH) * npad128(p.N);
-  const long long blocks = (rows + 7) / 8;
+  const long long row_blocks = (rows + 7) / 8;
+  const long long part4 = static_cast<long long>(p.n_split) * 2 * 128 * p.d / 4;
+  const long long blocks = row_blocks + (part4 + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fa_bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dO), p.lse, p.lse2, p.dsum,
-      p.dq_acc, p.BH, p.N, p.d, 1.f / p.scale, p.d == 64);
+      p.dq_acc, p.BH, p.N, p.d, 1.f / p.scale, p.d == 64, row_blocks, p.kv_part, part4);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t s) {
   const long long n8 = static_cast<long long>(p.BH) * p.N * p.d / 8;
-  if ((n8 + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
-      p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8, p.scale);
+  const long long total = n8 + static_cast<long long>(p.n_split) * 2 * 128 * p.d / 8;
+  if ((total + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fa_bwd_dq_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
+      p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), n8, p.scale, p.kv_part, static_cast<__nv_bfloat16*>(p.dk),
+      static_cast<__nv_bfloat16*>(p.dv), p.n_full, p.n_split, p.N, p.d);
   return cudaGetLastError();
 }
 

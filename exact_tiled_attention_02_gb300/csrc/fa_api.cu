@@ -171,7 +171,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
   const long long bh = static_cast<long long>(B) * H;
   if (bh > 0x7fffffffLL) return 0;
-  return bwd_workspace_layout(static_cast<int>(bh), N, d, nullptr, nullptr);
+  return bwd_workspace_layout(static_cast<int>(bh), N, d, nullptr, nullptr, nullptr);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -310,11 +310,14 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  size_t off_lse2 = 0, off_dsum = 0;
-  bwd_workspace_layout(B * H, N, d, &off_lse2, &off_dsum);
+  size_t off_lse2 = 0, off_dsum = 0, off_part = 0;
+  bwd_workspace_layout(B * H, N, d, &off_lse2, &off_dsum, &off_part);
   p.dq_acc = static_cast<float*>(workspace);
   p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_lse2);
   p.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_dsum);
+  p.kv_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_part);
+  p.n_full = 0;  // set by the bf16 launcher
+  p.n_split = 0;
   p.BH = B * H;
   p.N = N;
   p.d = d;

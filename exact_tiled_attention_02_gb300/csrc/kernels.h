@@ -44,6 +44,16 @@ struct BwdParams {
   // (-1e30 in padding rows) and of -D_i (0), then five zeros.
   float* lse2;
   float* dsum;
+  // Tail split of the bf16 backward at d = 96 and 128 without a window: the
+  // key tiles [n_full, n_full + n_split) of the (head, key tile) order run as
+  // two CTAs each, over the first and the second half of their query tiles,
+  // so that a last, partly filled wave of CTAs takes about half as long.
+  // Both halves add their fp32 dV and scale * dK rows into kv_part
+  // ([n_split][2][128][d], dV first; zeroed by the prep kernel), and the dQ
+  // kernel converts those rows to bf16.  n_split = 0: every tile is whole.
+  float* kv_part;
+  int n_full;
+  int n_split;
   int BH;
   int N;
   int d;
@@ -93,7 +103,7 @@ cudaError_t launch_bwd_main_d64(const BwdParams& p, const BwdMaps& m, unsigned g
 cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
 // Byte size of the backward workspace and the offsets of its lse2 / dsum
 // sections (dq_acc is at offset 0); rows are padded to multiples of 128.
-size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum);
+size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum, size_t* off_part);
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, cudaStream_t s);
 
 // Row counts of the tiles the TMA boxes use (host needs them for the maps).
@@ -101,5 +111,6 @@ constexpr int kFwdBlockRows = 128;  // query rows per CTA tile
 constexpr int kFwdBlockCols = 128;  // keys per K/V tile
 constexpr int kBwdBlockRows = 128;  // query rows per step of the backward
 constexpr int kBwdBlockCols = 128;  // keys per CTA of the backward
+constexpr int kMaxSplitTiles = 128;  // bound on BwdParams::n_split (sizes the kv_part workspace)
 
 }  // namespace fa

@@ -241,6 +241,12 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
+// The same for four consecutive floats (16-byte aligned address).
+__device__ __forceinline__ void red_add_v4_f32(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // TMA reduction: element-wise add of a shared-memory box into a 3-D tiled
 // global tensor (fp32 add performed by the memory system), tracked by the
 // issuing thread's bulk-async group.

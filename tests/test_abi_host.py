@@ -49,8 +49,12 @@ def test_workspace_size(b):
     assert n >= rows * 128 * 4 + rows * 4 and n % 256 == 0
     # dQ accumulator (15 floats -> 256 B), lse2 and D (128 padded rows each -> 512 B)
     assert b.fa_bwd_workspace_bytes(1, 1, 3, 5) == 256 + 512 + 512
-    assert b.fa_bwd_workspace_bytes(2, 1, 129, 128) == 2 * 129 * 128 * 4 + 2 * (2 * 256 * 4)
-    # d = 64: 16 bytes per padded row in the two row arrays
+    # d = 128: dV and dK partial rows of the 2 * 2 key tiles follow
+    assert b.fa_bwd_workspace_bytes(2, 1, 129, 128) == 2 * 129 * 128 * 4 + 2 * (2 * 256 * 4) + 4 * 2 * 128 * 128 * 4
+    assert b.fa_bwd_workspace_bytes(1, 1, 128, 96) == 128 * 96 * 4 + 2 * 512 + 1 * 2 * 128 * 96 * 4
+    # ... for at most 128 key tiles
+    assert b.fa_bwd_workspace_bytes(4, 16, 4096, 128) == 4 * 16 * 4096 * (128 * 4 + 2 * 4) + 128 * 2 * 128 * 128 * 4
+    # d = 64: 16 bytes per padded row in the two row arrays, no partial rows
     assert b.fa_bwd_workspace_bytes(2, 1, 129, 64) == 2 * 129 * 64 * 4 + 2 * (2 * 256 * 16)
 
 
