@@ -157,13 +157,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N, r = p.window_r;
   const int nkt = (N + BN - 1) / BN;
-  const int bh = blockIdx.x / nkt;
-  const int k0 = (blockIdx.x % nkt) * BN;
+  // CTAs past n_full take one half of a split key tile's query tiles each
+  int tile = static_cast<int>(blockIdx.x), half = -1;
+  if (tile >= p.n_full) {
+    half = (tile - p.n_full) & 1;
+    tile = p.n_full + ((tile - p.n_full) >> 1);
+  }
+  const int bh = tile / nkt;
+  const int k0 = (tile % nkt) * BN;
   const int np = npad128(N);
   int t_lo = 0, t_hi = (N + BM - 1) / BM;  // query tiles that can see this key tile
   if (r >= 0) {
     t_lo = max(0, k0 - r) / BM;
     t_hi = (min(N, k0 + BN + r) + BM - 1) / BM;
+  }
+  if (half >= 0) {
+    const int mid = t_lo + (t_hi - t_lo) / 2;
+    if (half == 0)
+      t_hi = mid;
+    else
+      t_lo = mid;
   }
   const int nsteps = t_hi - t_lo;
 
@@ -497,7 +510,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every product has completed
     const bool have = ok && warp_wait(bar.fin(), 0);
     const uint32_t stage_out = g == 0 ? sK : sV;
-    if (have) {
+    if (have && half >= 0) {
+      // one half of a split key tile: add this row's fp32 values into the
+      // partial rows (two addends into zeroed memory: order-independent)
+      tc_fence_after();
+      const uint32_t tcol = g == 0 ? TM_DV : TM_DK;
+      const float mul = g == 0 ? 1.f : p.scale;
+      float* dst = p.kv_part + ((static_cast<size_t>(tile - p.n_full) * 2 + g) * BN + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tl + tcol + c * 32, v);
+        tmem_wait_ld();
+        if (k0 + row < N) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4_f32(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                           __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+        }
+      }
+    } else if (have) {
       tc_fence_after();
       const uint32_t tcol = g == 0 ? TM_DV : TM_DK;
       const float mul = g == 0 ? 1.f : p.scale;
@@ -519,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     named_bar_sync(1 + g, 128);
-    if (have && !*abort_flag) {
+    if (have && half < 0 && !*abort_flag) {
       uint8_t* gout = reinterpret_cast<uint8_t*>(g == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * N + k0) * D * 2;
       constexpr int CHUNKS = D / 8;
       for (int idx = row; idx < BN * CHUNKS; idx += 128) {

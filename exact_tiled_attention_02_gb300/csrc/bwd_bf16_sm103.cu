@@ -630,10 +630,10 @@ cudaError_t launch_bwd_bf16_tc(const BwdParams& p_in, const BwdMaps& m, cudaStre
   const long long nkt = (p.N + BN - 1) / BN;
   const long long tiles = nkt * p.BH;
   // One CTA per SM.  When the last wave would hold at most half the SMs, its
-  // key tiles are split in two (d = 96, 128, no window, at least two query
-  // tiles): 2w half-length CTAs instead of w full ones.
+  // key tiles are split in two (no window, at least two query tiles): 2w
+  // half-length CTAs instead of w full ones.
   long long split = 0;
-  if (p.d != 64 && p.window_r < 0 && p.N > BM) {
+  if (p.window_r < 0 && p.N > BM) {
     const int sms = device_sm_count();
     const long long w = sms > 0 ? tiles % sms : 0;
     if (w > 0 && 2 * w <= sms && w <= kMaxSplitTiles) split = w;

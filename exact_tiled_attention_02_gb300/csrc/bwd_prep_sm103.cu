@@ -157,9 +157,9 @@ size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_
   const size_t acc = (rows * d * sizeof(float) + 255) & ~size_t(255);
   // d = 64 stores each row's value as three bf16 terms in a 16-byte row
   const size_t vec = (prow * (d == 64 ? 16 : sizeof(float)) + 255) & ~size_t(255);
-  // d = 96, 128: fp32 dV and dK rows of up to kMaxSplitTiles split key tiles
+  // bf16 head dimensions: fp32 dV and dK rows of up to kMaxSplitTiles split key tiles
   const size_t tiles = static_cast<size_t>(BH) * ((N + 127) / 128);
-  const size_t split = (d == 96 || d == 128) ? (tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles) : 0;
+  const size_t split = (d == 64 || d == 96 || d == 128) ? (tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles) : 0;
   const size_t part = split * 2 * 128 * d * sizeof(float);  // a multiple of 256
   if (off_lse2) *off_lse2 = acc;
   if (off_dsum) *off_dsum = acc + vec;

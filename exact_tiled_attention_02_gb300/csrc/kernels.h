@@ -44,7 +44,7 @@ struct BwdParams {
   // (-1e30 in padding rows) and of -D_i (0), then five zeros.
   float* lse2;
   float* dsum;
-  // Tail split of the bf16 backward at d = 96 and 128 without a window: the
+  // Tail split of the bf16 backward without a window: the
   // key tiles [n_full, n_full + n_split) of the (head, key tile) order run as
   // two CTAs each, over the first and the second half of their query tiles,
   // so that a last, partly filled wave of CTAs takes about half as long.

@@ -86,7 +86,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * from lse_i and from D_i = sum_k dO_ik O_ik (Npad = N rounded up to a
  * multiple of 128; 4 bytes per row, or 16 bytes per row at d = 64, where
  * each value is kept as three bf16 terms), each section 256-byte aligned;
- * at d = 96 and 128 then float32 dV and dK rows for up to 128 key tiles of
+ * at d = 64, 96 and 128 then float32 dV and dK rows for up to 128 key tiles of
  * 128 keys (min(B*H*ceil(N/128), 128) * 2 * 128 * d * 4 bytes), which the
  * backward uses when it splits the key tiles of a last, partly filled wave
  * of CTAs in two.  Returns 0 for non-positive sizes.

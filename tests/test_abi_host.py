@@ -54,8 +54,10 @@ def test_workspace_size(b):
     assert b.fa_bwd_workspace_bytes(1, 1, 128, 96) == 128 * 96 * 4 + 2 * 512 + 1 * 2 * 128 * 96 * 4
     # ... for at most 128 key tiles
     assert b.fa_bwd_workspace_bytes(4, 16, 4096, 128) == 4 * 16 * 4096 * (128 * 4 + 2 * 4) + 128 * 2 * 128 * 128 * 4
-    # d = 64: 16 bytes per padded row in the two row arrays, no partial rows
-    assert b.fa_bwd_workspace_bytes(2, 1, 129, 64) == 2 * 129 * 64 * 4 + 2 * (2 * 256 * 16)
+    # d = 64: 16 bytes per padded row in the two row arrays
+    assert b.fa_bwd_workspace_bytes(2, 1, 129, 64) == 2 * 129 * 64 * 4 + 2 * (2 * 256 * 16) + 4 * 2 * 128 * 64 * 4
+    # other head dimensions (fp32 only): no partial rows
+    assert b.fa_bwd_workspace_bytes(2, 1, 129, 32) == 2 * 129 * 32 * 4 + 2 * (2 * 256 * 4)
 
 
 def test_wait_limit_roundtrip(b):
