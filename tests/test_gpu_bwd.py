@@ -99,15 +99,37 @@ def test_bwd_elementwise(B, H, N, d, window, qk):
         _check_grad(name, _np(g), r, (B, H, N, d, window, qk))
 
 
-def test_bwd_deterministic_dk_dv():
-    """dK and dV are reduced on chip without atomics, so they are bitwise
-    repeatable; dQ (fp32 atomics) is repeatable to rounding."""
+@pytest.mark.parametrize("d", [64, 96, 128])
+def test_bwd_deterministic_dk_dv(d):
+    """dK and dV of a whole key tile are reduced on chip.  The key tiles of a
+    partly filled last wave run as two CTAs whose fp32 partial rows are added
+    into zeroed memory, and two addends sum the same in either order.  So dK
+    and dV are bitwise repeatable either way; dQ (fp32 reductions from many
+    CTAs) is repeatable to rounding.  1 x 2 x 333 has 6 key tiles, so on a
+    GPU with 12 or more SMs every tile is split (3 query tiles: halves of 1
+    and 2)."""
     dev = _dev()
-    q, k, v, do = inputs.make_inputs(1, 2, 333, 128, "bf16", seed=4, with_do=True)
-    a = _run(q, k, v, do, 1 / np.sqrt(128), 0, dev)
-    b = _run(q, k, v, do, 1 / np.sqrt(128), 0, dev)
+    q, k, v, do = inputs.make_inputs(1, 2, 333, d, "bf16", seed=4, with_do=True)
+    a = _run(q, k, v, do, 1 / np.sqrt(d), 0, dev)
+    b = _run(q, k, v, do, 1 / np.sqrt(d), 0, dev)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert _rel(_np(a[0]), _np(b[0])) <= 1e-3
+
+
+def test_bwd_split_last_wave_mixed():
+    """80 heads x 2 key tiles = 160 CTAs: on a 152-SM GB300 that is 152 whole
+    key tiles and a last wave of 8 tiles split in two.  Every head against
+    the oracle, and dK / dV bitwise repeatable."""
+    dev = _dev()
+    B, H, N, d = 1, 80, 256, 128
+    q, k, v, do = inputs.make_inputs(B, H, N, d, "bf16", seed=21, with_do=True)
+    scale = 1 / np.sqrt(d)
+    a = _run(q, k, v, do, scale, 0, dev)
+    b = _run(q, k, v, do, scale, 0, dev)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    refs = oracle.dense_backward(_np(q), _np(k), _np(v), _np(do), scale, 0)
+    for name, g, r in zip(("dq", "dk", "dv"), a, refs):
+        _check_grad(name, _np(g), r, (B, H, N, d, 0, 1.0))
 
 
 @pytest.mark.parametrize("d", [64, 96, 128])
