@@ -104,8 +104,10 @@ __device__ __forceinline__ void block_abt(float (&acc)[4][4], const float* a, in
 }
 
 // acc[i][m] += sum_r w[(4ty + i) * T + r] * b[(tx + 16 m) * LD + r] over the
-// 64 rows r of a tile: w row-major [64][64], b transposed with LD-float rows
-__device__ __forceinline__ void accum_wb(float (&acc)[4][8], const float* w, const float* b, int ty, int tx, bool hi) {
+// 64 rows r of a tile: w row-major [64][64], b transposed with LD-float rows;
+// M = 8 head-column slots (d up to 128) or 4 (d up to 64)
+template <int M>
+__device__ __forceinline__ void accum_wb(float (&acc)[4][M], const float* w, const float* b, int ty, int tx) {
 #pragma unroll 2
   for (int r4 = 0; r4 < T; r4 += 4) {
     float wv[4][4];
@@ -120,8 +122,7 @@ __device__ __forceinline__ void accum_wb(float (&acc)[4][8], const float* w, con
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        if (m >= 4 && !hi) break;
+      for (int m = 0; m < M; ++m) {
         const float bv = b[(tx + 16 * m) * LD + r4 + rr];
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i][m] = fmaf(wv[i][rr], bv, acc[i][m]);
@@ -130,31 +131,37 @@ __device__ __forceinline__ void accum_wb(float (&acc)[4][8], const float* w, con
   }
 }
 
-// shared memory of both tile kernels, in floats
-constexpr int SMEM_FLOATS = 2 * kMaxD * T + 2 * kMaxD * LD + 2 * T * T;
-constexpr int SMEM_BYTES = SMEM_FLOATS * 4;
+// shared memory of both tile kernels, in floats, for head dimensions up to
+// DR (128, or 64: then two CTAs fit on an SM)
+template <int DR>
+constexpr int smem_bytes() {
+  return (2 * DR * T + 2 * DR * LD + 2 * T * T) * 4;
+}
+static_assert(smem_bytes<64>() <= 113 * 1024, "two d <= 64 CTAs per SM");
 
 // ---------------------------------------------------------------------------
 // dK, dV: one CTA per 64 keys
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool HI>  // head columns 64.. exist (d > 64)
+__global__ void __launch_bounds__(kThreads, HI ? 1 : 2)
     fa_bwd_f32_dkdv_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
                            const float* __restrict__ lse, const float* __restrict__ dO,
                            const float* __restrict__ dsum, float* __restrict__ dk, float* __restrict__ dv, int N,
                            int d, int window_r, float scale) {
+  constexpr int DR = HI ? kMaxD : 64;  // head-dimension rows of the transposed tiles
+  constexpr int M = HI ? 8 : 4;        // head-column slots per thread
   extern __shared__ float4 smem4[];
   float* Kt = reinterpret_cast<float*>(smem4);  // [d][64]
-  float* Vt = Kt + kMaxD * T;                   // [d][64]
-  float* Qt = Vt + kMaxD * T;                   // [d][LD]
-  float* Gt = Qt + kMaxD * LD;                  // dO, [d][LD]
-  float* Ps = Gt + kMaxD * LD;                  // P^T [64 keys][64 queries]
+  float* Vt = Kt + DR * T;                      // [d][64]
+  float* Qt = Vt + DR * T;                      // [d][LD]
+  float* Gt = Qt + DR * LD;                     // dO, [d][LD]
+  float* Ps = Gt + DR * LD;                     // P^T [64 keys][64 queries]
   float* Ss = Ps + T * T;                       // dS^T [64 keys][64 queries]
   const int nkt = (N + T - 1) / T;
   const long long bh = blockIdx.x / nkt;
   const int k0 = (blockIdx.x % nkt) * T;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int dp = (d + 3) & ~3;
-  const bool hi = dp > 64;  // head columns 64.. exist
   const long long head = bh * static_cast<long long>(N) * d;
   load_t(Kt, T, k + head, k0, N, d, dp);
   load_t(Vt, T, v + head, k0, N, d, dp);
@@ -163,11 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     i_lo = max(0, k0 - window_r);
     i_hi = min(N, k0 + T - 1 + window_r + 1);
   }
-  float acc_k[4][8], acc_v[4][8];
+  float acc_k[4][M], acc_v[4][M];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < M; ++m) {
       acc_k[i][m] = 0.f;
       acc_v[i][m] = 0.f;
     }
@@ -199,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float4*>(Ss + (4 * ty + ii) * T + 4 * tx) = make_float4(g[ii][0], g[ii][1], g[ii][2], g[ii][3]);
     }
     __syncthreads();
-    accum_wb(acc_v, Ps, Gt, ty, tx, hi);  // dV += P^T dO
-    accum_wb(acc_k, Ss, Qt, ty, tx, hi);  // dK += dS^T Q
+    accum_wb<M>(acc_v, Ps, Gt, ty, tx);  // dV += P^T dO
+    accum_wb<M>(acc_k, Ss, Qt, ty, tx);  // dK += dS^T Q
   }
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
@@ -209,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* krow = dk + head + static_cast<long long>(j) * d;
     float* vrow = dv + head + static_cast<long long>(j) * d;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < M; ++m) {
       const int c = tx + 16 * m;
       if (c < d) {
         krow[c] = acc_k[ii][m] * scale;
@@ -222,23 +229,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // dQ: one CTA per 64 queries
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool HI>
+__global__ void __launch_bounds__(kThreads, HI ? 1 : 2)
     fa_bwd_f32_dq_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
                          const float* __restrict__ lse, const float* __restrict__ dO,
                          const float* __restrict__ dsum, float* __restrict__ dq, int N, int d, int window_r,
                          float scale) {
+  constexpr int DR = HI ? kMaxD : 64;
+  constexpr int M = HI ? 8 : 4;
   extern __shared__ float4 smem4[];
   float* Qt = reinterpret_cast<float*>(smem4);  // [d][64]
-  float* Gt = Qt + kMaxD * T;                   // dO, [d][64]
-  float* Kt = Gt + kMaxD * T;                   // [d][LD]
-  float* Vt = Kt + kMaxD * LD;                  // [d][LD]
-  float* Ss = Vt + kMaxD * LD;                  // dS [64 queries][64 keys]
+  float* Gt = Qt + DR * T;                      // dO, [d][64]
+  float* Kt = Gt + DR * T;                      // [d][LD]
+  float* Vt = Kt + DR * LD;                     // [d][LD]
+  float* Ss = Vt + DR * LD;                     // dS [64 queries][64 keys]
   const int nqt = (N + T - 1) / T;
   const long long bh = blockIdx.x / nqt;
   const int q0 = (blockIdx.x % nqt) * T;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int dp = (d + 3) & ~3;
-  const bool hi = dp > 64;
   const long long head = bh * static_cast<long long>(N) * d;
   load_t(Qt, T, q + head, q0, N, d, dp);
   load_t(Gt, T, dO + head, q0, N, d, dp);
@@ -254,11 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     l_i[ii] = i < N ? lse[bh * N + i] : 0.f;
     d_i[ii] = i < N ? dsum[bh * N + i] : 0.f;
   }
-  float acc[4][8];
+  float acc[4][M];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[i][m] = 0.f;
+    for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
   for (int k0 = (j_lo / T) * T; k0 < j_hi; k0 += T) {
     __syncthreads();  // the previous tile's K, V, dS are no longer read
     load_t(Kt, LD, k + head, k0, N, d, dp);
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float4*>(Ss + (4 * ty + ii) * T + 4 * tx) = make_float4(g[ii][0], g[ii][1], g[ii][2], g[ii][3]);
     }
     __syncthreads();
-    accum_wb(acc, Ss, Kt, ty, tx, hi);  // dQ += dS K
+    accum_wb<M>(acc, Ss, Kt, ty, tx);  // dQ += dS K
   }
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
@@ -288,11 +297,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (i >= N) continue;
     float* qrow = dq + head + static_cast<long long>(i) * d;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < M; ++m) {
       const int c = tx + 16 * m;
       if (c < d) qrow[c] = acc[ii][m] * scale;
     }
   }
+}
+
+}  // namespace
+
+namespace {
+
+// the two tile kernels for head dimensions up to 64 (HI = false) or 128
+template <bool HI>
+cudaError_t launch_tiles(const BwdParams& p, long long tiles, cudaStream_t s) {
+  constexpr int SMEM = smem_bytes<HI ? kMaxD : 64>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_f32_dkdv_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_bwd_f32_dq_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const float* q = static_cast<const float*>(p.q);
+  const float* k = static_cast<const float*>(p.k);
+  const float* v = static_cast<const float*>(p.v);
+  const float* dO = static_cast<const float*>(p.dO);
+  fa_bwd_f32_dq_kernel<HI><<<static_cast<unsigned>(tiles), kThreads, SMEM, s>>>(
+      q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dq), p.N, p.d, p.window_r, p.scale);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fa_bwd_f32_dkdv_kernel<HI><<<static_cast<unsigned>(tiles), kThreads, SMEM, s>>>(
+      q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dk), static_cast<float*>(p.dv), p.N, p.d, p.window_r,
+      p.scale);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -303,31 +342,12 @@ cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s) {
   const long long prep_blocks = (rows + kPrepWarps - 1) / kPrepWarps;
   const long long tiles = static_cast<long long>(p.BH) * ((p.N + T - 1) / T);
   if (prep_blocks > 0x7fffffffLL || tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_f32_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_bwd_f32_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const float* q = static_cast<const float*>(p.q);
-  const float* k = static_cast<const float*>(p.k);
-  const float* v = static_cast<const float*>(p.v);
-  const float* dO = static_cast<const float*>(p.dO);
   // D_i uses the workspace's D section as a plain [B*H*N] array
   fa_bwd_f32_prep_kernel<<<static_cast<unsigned>(prep_blocks), kPrepWarps * 32, 0, s>>>(
-      static_cast<const float*>(p.o), dO, p.dsum, rows, p.d);
+      static_cast<const float*>(p.o), static_cast<const float*>(p.dO), p.dsum, rows, p.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_f32_dq_kernel<<<static_cast<unsigned>(tiles), kThreads, SMEM_BYTES, s>>>(
-      q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dq), p.N, p.d, p.window_r, p.scale);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  fa_bwd_f32_dkdv_kernel<<<static_cast<unsigned>(tiles), kThreads, SMEM_BYTES, s>>>(
-      q, k, v, p.lse, dO, p.dsum, static_cast<float*>(p.dk), static_cast<float*>(p.dv), p.N, p.d, p.window_r,
-      p.scale);
-  return cudaGetLastError();
+  return ((p.d + 3) & ~3) > 64 ? launch_tiles<true>(p, tiles, s) : launch_tiles<false>(p, tiles, s);
 }
 
 }  // namespace fa
