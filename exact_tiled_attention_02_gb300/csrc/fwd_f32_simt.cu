@@ -28,8 +28,12 @@ constexpr int BQ = 64;        // query rows per CTA
 constexpr int BK = 64;        // keys per tile
 constexpr int kThreads = 256;
 constexpr int kMaxD = 128;
-constexpr int SMEM_FLOATS = kMaxD * BQ + kMaxD * BK + BK * kMaxD + BQ * BK;  // Qt, Kt, Vs, Ps
-constexpr int SMEM_BYTES = SMEM_FLOATS * 4;                                  // 112 KB: two CTAs per SM
+// shared memory for head dimensions up to DR (Qt, Kt, Vs, Ps): 112 KB at
+// DR = 128 (two CTAs per SM), 64 KB at DR = 64 (three)
+template <int DR>
+constexpr int smem_bytes() {
+  return (DR * BQ + DR * BK + BK * DR + BQ * BK) * 4;
+}
 
 __device__ __forceinline__ float half_warp_max(float x) {
 #pragma unroll
@@ -44,10 +48,11 @@ __device__ __forceinline__ float half_warp_sum(float x) {
 }
 
 // rows [r0, r0 + 64) of a [N][d] matrix into shared memory: transposed
-// (dst[c][row], 64 floats per c) or row-major (dst[row][c], kMaxD floats per
+// (dst[c][row], 64 floats per c) or row-major (dst[row][c], ldr floats per
 // row), columns up to dp (d rounded up to 4), zero past N and past d
 template <bool TRANSPOSE>
-__device__ __forceinline__ void load_tile(float* dst, const float* __restrict__ src, int r0, int N, int d, int dp) {
+__device__ __forceinline__ void load_tile(float* dst, const float* __restrict__ src, int r0, int N, int d, int dp,
+                                          int ldr) {
   const int tid = threadIdx.x;
   if ((d & 3) == 0) {
     const int c4n = dp >> 2;
@@ -61,7 +66,7 @@ __device__ __forceinline__ void load_tile(float* dst, const float* __restrict__ 
         dst[(4 * c4 + 2) * 64 + row] = v.z;
         dst[(4 * c4 + 3) * 64 + row] = v.w;
       } else {
-        *reinterpret_cast<float4*>(dst + row * kMaxD + 4 * c4) = v;
+        *reinterpret_cast<float4*>(dst + row * ldr + 4 * c4) = v;
       }
     }
   } else {
@@ -71,19 +76,22 @@ __device__ __forceinline__ void load_tile(float* dst, const float* __restrict__ 
       if (TRANSPOSE)
         dst[c * 64 + row] = v;
       else
-        dst[row * kMaxD + c] = v;
+        dst[row * ldr + c] = v;
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+template <bool HI>  // output columns 64.. exist (d > 64)
+__global__ void __launch_bounds__(kThreads, HI ? 2 : 3)
     fa_fwd_f32_simt_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
                            float* __restrict__ o, float* __restrict__ lse, int N, int d, int window_r, float scale) {
+  constexpr int DR = HI ? kMaxD : 64;  // head-dimension extent of the tiles
+  constexpr int M = HI ? 8 : 4;        // output columns per thread
   extern __shared__ float4 smem4[];
-  float* Qt = reinterpret_cast<float*>(smem4);  // [kMaxD][64]
-  float* Kt = Qt + kMaxD * BQ;                  // [kMaxD][64]
-  float* Vs = Kt + kMaxD * BK;                  // [64][kMaxD]
-  float* Ps = Vs + BK * kMaxD;                  // [64][64]
+  float* Qt = reinterpret_cast<float*>(smem4);  // [DR][64]
+  float* Kt = Qt + DR * BQ;                     // [DR][64]
+  float* Vs = Kt + DR * BK;                     // [64][DR]
+  float* Ps = Vs + BK * DR;                     // [64][64]
   const int nqt = (N + BQ - 1) / BQ;
   const long long bh = blockIdx.x / nqt;
   const int q0 = (blockIdx.x % nqt) * BQ;
@@ -94,26 +102,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float* kh = k + head;
   const float* vh = v + head;
 
-  load_tile<true>(Qt, qh, q0, N, d, dp);
+  load_tile<true>(Qt, qh, q0, N, d, dp, DR);
 
   int j_lo = 0, j_hi = N;  // keys that some row of this CTA sees
   if (window_r >= 0) {
     j_lo = max(0, q0 - window_r);
     j_hi = min(N, q0 + BQ - 1 + window_r + 1);
   }
-  float m[4], l[4], acc[4][8];
+  float m[4], l[4], acc[4][M];
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
     m[ii] = -INFINITY;
     l[ii] = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[ii][c] = 0.f;
+    for (int c = 0; c < M; ++c) acc[ii][c] = 0.f;
   }
-  const bool hi_half = dp > 64;  // output columns 64.. exist
   for (int k0 = (j_lo / BK) * BK; k0 < j_hi; k0 += BK) {
     __syncthreads();  // the previous tile's K, V and P are no longer read
-    load_tile<true>(Kt, kh, k0, N, d, dp);
-    load_tile<false>(Vs, vh, k0, N, d, dp);
+    load_tile<true>(Kt, kh, k0, N, d, dp, DR);
+    load_tile<false>(Vs, vh, k0, N, d, dp, DR);
     __syncthreads();
     // ---- S = Q K^T for rows 4ty.., keys 4tx..
     float s[4][4];
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       l[ii] = l[ii] * alpha + half_warp_sum(rs);
       m[ii] = m_new;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[ii][c] *= alpha;
+      for (int c = 0; c < M; ++c) acc[ii][c] *= alpha;
       *reinterpret_cast<float4*>(Ps + (4 * ty + ii) * BK + 4 * tx) = make_float4(pv[0], pv[1], pv[2], pv[3]);
     }
     __syncthreads();
@@ -173,14 +180,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const float4 v0 = *reinterpret_cast<const float4*>(Vs + (k4 + kk) * kMaxD + 4 * tx);
+        const float4 v0 = *reinterpret_cast<const float4*>(Vs + (k4 + kk) * DR + 4 * tx);
         const float vv0[4] = {v0.x, v0.y, v0.z, v0.w};
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[ii][c] = fmaf(p[ii][kk], vv0[c], acc[ii][c]);
-        if (hi_half) {
-          const float4 v1 = *reinterpret_cast<const float4*>(Vs + (k4 + kk) * kMaxD + 64 + 4 * tx);
+        if constexpr (HI) {
+          const float4 v1 = *reinterpret_cast<const float4*>(Vs + (k4 + kk) * DR + 64 + 4 * tx);
           const float vv1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
           for (int ii = 0; ii < 4; ++ii)
@@ -200,10 +207,30 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       if (4 * tx + c < d) orow[4 * tx + c] = acc[ii][c] * inv;
-      if (64 + 4 * tx + c < d) orow[64 + 4 * tx + c] = acc[ii][4 + c] * inv;
+      if constexpr (HI)
+        if (64 + 4 * tx + c < d) orow[64 + 4 * tx + c] = acc[ii][4 + c] * inv;
     }
     if (lse != nullptr && tx == 0) lse[bh * N + i] = m[ii] + logf(l[ii]);
   }
+}
+
+}  // namespace
+
+namespace {
+
+template <bool HI>
+cudaError_t launch_hi(const FwdParams& p, long long blocks, cudaStream_t s) {
+  constexpr int SMEM = smem_bytes<HI ? kMaxD : 64>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_f32_simt_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  fa_fwd_f32_simt_kernel<HI><<<static_cast<unsigned>(blocks), kThreads, SMEM, s>>>(
+      static_cast<const float*>(p.q), static_cast<const float*>(p.k), static_cast<const float*>(p.v),
+      static_cast<float*>(p.o), p.lse, p.N, p.d, p.window_r, p.scale);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -212,16 +239,7 @@ cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s) {
   if (p.d > kMaxD || p.d < 1) return cudaErrorInvalidConfiguration;
   const long long blocks = static_cast<long long>(p.BH) * ((p.N + BQ - 1) / BQ);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_f32_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  fa_fwd_f32_simt_kernel<<<static_cast<unsigned>(blocks), kThreads, SMEM_BYTES, s>>>(
-      static_cast<const float*>(p.q), static_cast<const float*>(p.k), static_cast<const float*>(p.v),
-      static_cast<float*>(p.o), p.lse, p.N, p.d, p.window_r, p.scale);
-  return cudaGetLastError();
+  return ((p.d + 3) & ~3) > 64 ? launch_hi<true>(p, blocks, s) : launch_hi<false>(p, blocks, s);
 }
 
 }  // namespace fa
