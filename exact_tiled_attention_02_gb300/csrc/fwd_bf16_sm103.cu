@@ -59,7 +59,25 @@ using namespace sm103;
 
 constexpr int BR = kFwdBlockRows;  // rows per query tile (two per item)
 constexpr int BC = kFwdBlockCols;  // keys per K/V tile
-constexpr int kThreads = 384;
+// The unmasked d = 128 instantiation adds a fourth warpgroup (warps 12-15)
+// that rescales O when a row's reference maximum moves, so that the softmax
+// warps need not.  Measured on 2x16x8192x128 with Q,K x8 (frequent
+// rescales): forward 0.758 -> 0.727 ms; with few rescales (standard-normal
+// inputs) it cost 1.5% at d = 128 and 1.3-3.3% at d = 96 and 64, which keep
+// the rescale in the softmax warps.
+template <int D, bool WIN>
+constexpr bool corr_warps() {
+  return !WIN && D == 128;  // the alpha region in shared memory exists only at D = 128
+}
+template <int D, bool WIN>
+constexpr int threads_for() {
+  return corr_warps<D, WIN>() ? 512 : 384;
+}
+// register shares with the correction warpgroup (512 threads x 128 at
+// launch): softmax warpgroups 152, the other two 104 (2 x 152 + 2 x 104 = 4 x 128)
+constexpr int kRegsSoftmax = 152;
+constexpr int kRegsOther = 104;
+static_assert(2 * kRegsSoftmax + 2 * kRegsOther == 4 * 128, "register shares must add up to the launch allocation");
 constexpr int kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;    // + 128 * tile
 constexpr uint32_t kTmemO = 256;  // + 128 * tile
@@ -123,14 +141,17 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   // q_full[2], q_empty[2], k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain,
-  // o_staged[2], o_free
-  static constexpr int NBAR = 4 + 3 * STAGES + 10;
+  // o_staged[2], o_free, alpha_ready[2]
+  static constexpr int NBAR = 4 + 3 * STAGES + 12;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // D = 64 leaves room for an output staging tile (bf16 [BR][DP]) that the
   // two query tiles share in turn; at DP = 128 the K/V ring takes that space
   static constexpr bool STAGED_OUT = (DP == 64);
-  static constexpr int OFF_OST = (OFF_MISC + 16 + 127) / 128 * 128;
-  static constexpr int SMEM_USED = STAGED_OUT ? OFF_OST + BR * DP * 2 : OFF_MISC + 16;
+  // each row's rescale factor, handed from the softmax to the correction
+  // warps (d = 128 only; elsewhere the extra shared memory cost L1 and time)
+  static constexpr int OFF_ALPHA = (OFF_MISC + 16 + 127) / 128 * 128;  // float [2][BR]
+  static constexpr int OFF_OST = OFF_ALPHA + (D == 128 ? 2 * BR * 4 : 0);
+  static constexpr int SMEM_USED = STAGED_OUT ? OFF_OST + BR * DP * 2 : OFF_OST;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(D % 32 == 0 && DP <= 128, "tensor memory budget");
@@ -150,6 +171,7 @@ struct Bars {
   __device__ uint32_t drain() const { return base + 8 * (10 + 3 * STAGES); }
   __device__ uint32_t o_staged(int t) const { return base + 8 * (11 + 3 * STAGES + t); }
   __device__ uint32_t o_free() const { return base + 8 * (13 + 3 * STAGES); }
+  __device__ uint32_t alpha_ready(int t) const { return base + 8 * (14 + 3 * STAGES + t); }
 };
 
 // The key tiles of one item: [j_lo, j_lo + ntiles), and each query tile's own
@@ -189,7 +211,7 @@ __device__ __forceinline__ Item decode_item(int item, int N, int r) {
 }
 
 template <int D, bool WIN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
     fa_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                                      const __grid_constant__ CUtensorMap tmv, const FwdParams p, int n_items) {
   using C = Cfg<D>;
@@ -217,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar.q_full(t), 1);
       mbar_init(bar.q_empty(t), 1);
       mbar_init(bar.s_full(t), 1);
-      mbar_init(bar.p_full(t), 4);
+      mbar_init(bar.p_full(t), corr_warps<D, WIN>() ? 8 : 4);  // the tile's softmax warps (+ correction warps)
+      mbar_init(bar.alpha_ready(t), 4);
       mbar_init(bar.o_done(t), 1);
     }
     for (int s = 0; s < C::STAGES; ++s) {
@@ -242,9 +265,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 10) {
-    // idle warps of the third warpgroup
-  } else if (warp == 9) {
+  // The roles, one lambda each.  Unmasked d = 128 adds the correction warps
+  // and moves registers between warpgroups (one setmaxnreg instruction per
+  // warpgroup, at the top of its branch); the other instantiations keep the
+  // twelve-warp layout, whose code measured faster there.
+  auto role_correction = [&]() {
+    // ------------------------------------------------------------ correction
+    // (unmasked d = 128) Warp 12 + q rescales the O rows in TMEM lane
+    // quarter q of both query tiles when a row's reference maximum has
+    // moved: after the tile's previous P V into O has completed and before
+    // its next one (p_full counts these warps too), while the softmax warps
+    // go on computing P.
+    if constexpr (corr_warps<D, WIN>()) {
+      const int q = warp & 3;
+      const uint32_t tlq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      const float* sAlpha = reinterpret_cast<const float*>(smem + C::OFF_ALPHA);
+      auto warp_wait = [&](uint32_t bar_addr, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
+      };
+      int nt[2] = {0, 0};  // key tiles each query tile has passed (all items)
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const Item w = decode_item<WIN>(item, N, r);
+        for (int it = 0; ok && it < w.ntiles; ++it) {
+          for (int t = 0; t < 2; ++t) {
+            if (it < w.lo[t] || it >= w.hi[t]) continue;
+            if (!warp_wait(bar.alpha_ready(t), nt[t] & 1)) {
+              ok = false;
+              break;
+            }
+            const float a = sAlpha[t * BR + q * 32 + lane];
+            if (it > w.lo[t] && __any_sync(0xffffffffu, a != 1.f)) {
+              if (!warp_wait(bar.o_done(t), (nt[t] - 1) & 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t tO = tlq + kTmemO + t * 128;
+              const float2 a2 = make_float2(a, a);
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tO + c * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                  o[e] = __float_as_uint(v.x);
+                  o[e + 1] = __float_as_uint(v.y);
+                }
+                tmem_st_32x32b_x32(tO + c * 32, o);
+              }
+              tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.p_full(t));
+            ++nt[t];
+          }
+        }
+      }
+    }
+  };
+  auto role_tma = [&]() {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       prefetch_tensormap(&tmq);
@@ -297,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 8) {
-    // ------------------------------------------------------------------ MMA
+  };
+  auto role_mma = [&]() {
+    // ------------------------------------------------------------------ MMA (warp 8)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BR, BC, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, C::DP, 0, 1);
@@ -452,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar.drain(), 0, drain);
     }
     __syncwarp();
-  } else {
+  };
+  auto role_softmax = [&]() {
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const int row = threadIdx.x & 127;
@@ -511,6 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = ex2_approx(m_ref - mt);
           m_ref = mt;
         }
+        if constexpr (corr_warps<D, WIN>()) {
+          // the correction warp of this lane quarter rescales O meanwhile
+          reinterpret_cast<float*>(smem + C::OFF_ALPHA)[t * BR + row] = alpha;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar.alpha_ready(t));
+        }
         const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
         const float2 sl2 = make_float2(sl, sl), nref2 = make_float2(nref, nref);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -530,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y) + (rs[2].x + rs[2].y) + (rs[3].x + rs[3].y);
         // O may be rescaled only once this item's previous P V into it has
         // completed (the first tile of an item starts a fresh O)
-        if (it > w.lo[t] && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!corr_warps<D, WIN>() && it > w.lo[t] && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
             tmem_wait_st();
             ok = false;
@@ -653,6 +744,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar.o_free());
       }
     }
+  };
+  if constexpr (corr_warps<D, WIN>()) {
+    if (warp >= 8) {
+      regs_decrease<kRegsOther>();
+      if (warp >= 12)
+        role_correction();
+      else if (warp == 9)
+        role_tma();
+      else if (warp == 8)
+        role_mma();
+    } else {
+      regs_increase<kRegsSoftmax>();
+      role_softmax();
+    }
+  } else {
+    if (warp >= 10) {
+      // idle warps of the third warpgroup
+    } else if (warp == 9) {
+      role_tma();
+    } else if (warp == 8) {
+      role_mma();
+    } else {
+      role_softmax();
+    }
   }
 
   tc_fence_before();
@@ -685,7 +800,7 @@ cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = static_cast<int>(items < sms ? items : sms);
-  fa_fwd_bf16_sm103_kernel<D, WIN><<<grid, kThreads, C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p,
+  fa_fwd_bf16_sm103_kernel<D, WIN><<<grid, threads_for<D, WIN>(), C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p,
                                                                                  static_cast<int>(items));
   return cudaGetLastError();
 }
