@@ -27,13 +27,15 @@
 //     staged in the Q buffer, which by then holds the next item's Q.
 // (Measured against one item per CTA: identical results bit for bit, 2.6% to
 // 7% faster on long key loops, 24% on the window-257 workload.)
-// 384 threads:
+// 384 threads (512 for unmasked d = 128):
 //   warps 0-3  softmax for Q0: thread t owns row t of Q0 (TMEM lane t)
 //   warps 4-7  softmax for Q1: thread t owns row t of Q1 (TMEM lane t)
 //   warp  8    TMEM owner + tcgen05.mma issuer (one elected lane)
 //   warp  9    TMA producer (one elected lane)
 //   warps 10-11 idle (registers are granted per warpgroup of four warps, so
 //              a ten-warp CTA costs as much as twelve; 168 per thread)
+//   warps 12-15 (unmasked d = 128) rescale O when a row's reference maximum
+//              moves, one warp per TMEM lane quarter (see corr_warps)
 // Tensor memory (512 columns x 128 lanes, 32-bit):
 //   [0,128) S0 (P0 as packed bf16 in its first 64 columns), [128,256) S1 / P1,
 //   [256,256+DP) O0, [384,384+DP) O1 (DP = D rounded up to 64: see Cfg).
