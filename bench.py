@@ -287,15 +287,14 @@ def main():
     dqd, dkd, dvd = (torch.empty_like(qd) for _ in range(3))
     ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
 
-    # does this build have the backward?
+    # The library has no backward for bf16 d = 256 only; such a problem is
+    # timed forward only and its metric says so.  For every other head
+    # dimension a refusal is an error, never a silent forward-only line.
+    if with_bwd and w.dtype == "bf16" and w.d == 256:
+        with_bwd = False
     if with_bwd:
-        try:
-            fa.fa_bwd(qd, kd, vd, *fa.fa_fwd(qd, kd, vd, scale=w.scale, window=w.window), dod, scale=w.scale,
-                      window=w.window, dq=dqd, dk=dkd, dv=dvd, workspace=ws)
-        except fa.FaError as e:
-            if e.status != fa.FA_ERR_UNSUPPORTED:
-                raise
-            with_bwd = False
+        fa.fa_bwd(qd, kd, vd, *fa.fa_fwd(qd, kd, vd, scale=w.scale, window=w.window), dod, scale=w.scale,
+                  window=w.window, dq=dqd, dk=dkd, dv=dvd, workspace=ws)
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()

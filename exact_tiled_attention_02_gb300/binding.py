@@ -269,10 +269,13 @@ def fa_bwd_static_workspace(q, k, v, o, lse, do, dq, dk, dv, scale: float | None
     (the caller passes the dq, dk, dv outputs).  Calls that overlap on the GPU
     share that array and race; problems needing more than 64 MiB of workspace
     raise FaError(FA_ERR_UNSUPPORTED)."""
+    torch = _torch()
     _check_qkv(q, k, v, o, do, dq, dk, dv)
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N:
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     st = lib.fa_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
                                      _ptr(dv), B, H, N, d, float(scale), int(window), _dtype_code(q),
                                      _stream_ptr(stream))

@@ -115,6 +115,25 @@ fa_status check_common(int B, int H, int N, int d, float scale, int window, fa_d
 
 int radius(int window) { return window > 0 ? (window - 1) / 2 : -1; }
 
+}  // namespace
+
+// Every check fa_bwd makes on its arguments other than the workspace: null
+// and misaligned pointers, sizes, scale, window, dtype, and the head
+// dimensions the backward does not implement.
+fa_status check_bwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, const void* dq, const void* dk, const void* dv, int B, int H, int N, int d,
+                         float scale, int window, fa_dtype dt) {
+  const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv, lse};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID;
+  const fa_status c = check_common(B, H, N, d, scale, window, dt);
+  if (c != FA_OK) return c;
+  if (dt == FA_DTYPE_BF16 && d == 256) return FA_ERR_UNSUPPORTED;  // forward only at d = 256
+  return FA_OK;
+}
+
+namespace {
+
 unsigned long long wait_ns() { return static_cast<unsigned long long>(g_wait_limit_us.load()) * 1000ull; }
 
 // Device-side self-test of the bounded wait: one thread waits on a barrier
@@ -290,15 +309,11 @@ fa_status fa_fwd_f32_3xtf32(const float* q, const float* k, const float* v, floa
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int window, fa_dtype dt,
                  void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID;
-  const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv, lse};
-  for (const void* ptr : ptrs)
-    if (!aligned16(ptr)) return FA_ERR_INVALID;
+  if (!workspace) return FA_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID;
-  const fa_status c = check_common(B, H, N, d, scale, window, dt);
+  const fa_status c = check_bwd_args(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, window, dt);
   if (c != FA_OK) return c;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
-  if (dt == FA_DTYPE_BF16 && d == 256) return FA_ERR_UNSUPPORTED;  // forward only at d = 256
 
   BwdParams p{};
   p.q = q;

@@ -14,8 +14,13 @@
 //   * the array holds kNoAllocScratchBytes (64 MiB); problems whose
 //     fa_bwd_workspace_bytes() exceeds that are refused with
 //     FA_ERR_UNSUPPORTED before anything runs;
-//   * every GPU that loads the library reserves the array until the process
-//     exits;
+//   * the array belongs to this file's module of device code.  Under CUDA's
+//     lazy module loading (the default) that module is loaded on a device,
+//     and the 64 MiB committed there, by the first call on that device (the
+//     address lookup below); with eager loading, when the library's code is
+//     loaded onto the device.  Either way it stays until the process exits.
+//     The first call may therefore allocate and synchronise inside the
+//     driver: make it outside any region where that is not allowed;
 //   * all calls share the one array, so calls whose work overlaps on the GPU
 //     (for example on two concurrently running streams) race on it and give
 //     wrong results; calls issued in order on one stream are fine.  Every
@@ -25,12 +30,15 @@
 //   * the array's device address is looked up (cudaGetSymbolAddress) by the
 //     first call on each device, with that device current; make that first
 //     call before any stream capture.
+//   * arguments are checked exactly as fa_bwd checks them (same status
+//     codes), before the size limit.
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "fa.h"
+#include "kernels.h"
 
 namespace {
 
@@ -74,7 +82,11 @@ extern "C" {
 fa_status fa_bwd_static_workspace(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                                   float scale, int window, fa_dtype dt, void* stream) {
-  // size check first: nothing touches the device for a request that cannot fit
+  // fa_bwd's own argument checks first, so a bad argument gets the status
+  // fa_bwd would give it whatever the problem's size; then the size limit.
+  // Neither touches the device.
+  const fa_status c = fa::check_bwd_args(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, window, dt);
+  if (c != FA_OK) return c;
   const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
   if (need == 0) return FA_ERR_INVALID;
   if (need > kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;

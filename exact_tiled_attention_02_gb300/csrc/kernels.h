@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Arguments shared by every forward kernel.  Arrays are [B,H,N,d] row-major;
@@ -105,6 +107,11 @@ cudaError_t launch_bwd_f32_simt(const BwdParams& p, cudaStream_t s);
 // sections (dq_acc is at offset 0); rows are padded to multiples of 128.
 size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_dsum, size_t* off_part);
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, cudaStream_t s);
+// fa_bwd's host-side argument checks, without those of the workspace
+// (fa_api.cu); FA_OK or the status fa_bwd would return.
+fa_status check_bwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, const void* dq, const void* dk, const void* dv, int B, int H, int N, int d,
+                         float scale, int window, fa_dtype dt);
 
 // Row counts of the tiles the TMA boxes use (host needs them for the maps).
 constexpr int kFwdBlockRows = 128;  // query rows per CTA tile

@@ -166,11 +166,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * fa_bwd for callers that cannot allocate device memory (code running where
  * device allocation is not permitted, or with no allocator to call): the same
  * arguments and results as fa_bwd, minus the workspace, which is replaced by
- * a fixed 64 MiB scratch array inside the library (reserved on every GPU that
- * loads the library, until the process exits).  This function allocates
- * nothing.  The pages describe no such variant; it is a deployment aid.
- *   - Problems with fa_bwd_workspace_bytes(B,H,N,d) > 64 MiB return
- *     FA_ERR_UNSUPPORTED before anything is launched.
+ * a fixed 64 MiB scratch array inside the library.  This function calls no
+ * allocator.  The pages describe no such variant; it is a deployment aid.
+ *   - Arguments are checked as fa_bwd checks them, with the same status
+ *     codes; then problems with fa_bwd_workspace_bytes(B,H,N,d) > 64 MiB
+ *     return FA_ERR_UNSUPPORTED.  Nothing is launched in either case.
+ *   - Under CUDA's lazy module loading (the default), the array is brought
+ *     onto a device, and its 64 MiB committed there, by the first call on
+ *     that device; it then stays until the process exits.  That first call
+ *     may therefore allocate and synchronise inside the CUDA driver: make it
+ *     outside any region where allocation or stream capture is forbidden.
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (e.g. on two concurrent streams) race on it; calls in order on one
  *     stream are fine.  Each call re-initialises what must start at zero.

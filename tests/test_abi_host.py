@@ -101,6 +101,29 @@ def test_bwd_rejects_on_host(b, kw, code):
     assert bwd(b, **kw) == code
 
 
+def bwd_static(b, q=P, lse=P, dt=1, B=1, H=1, N=8, d=128, window=0, scale=0.1):
+    vp = ctypes.c_void_p
+    return b.lib.fa_bwd_static_workspace(vp(q), vp(P), vp(P), vp(P), vp(lse), vp(P), vp(P), vp(P), vp(P), B, H, N, d,
+                                         scale, window, dt, vp(0))
+
+
+BIG = dict(B=4, H=16, N=16384)  # needs far more than the 64 MiB static scratch
+
+
+@pytest.mark.parametrize("kw,code", [
+    # invalid arguments get fa_bwd's status whatever the problem's size
+    (dict(q=0, **BIG), 1), (dict(lse=0, **BIG), 1), (dict(q=P + 8, **BIG), 1), (dict(dt=7, **BIG), 1),
+    (dict(window=4, **BIG), 1), (dict(scale=0.0, **BIG), 1), (dict(B=0), 1),
+    (dict(q=0), 1), (dict(dt=7), 1),
+    # backward not implemented for these head dimensions, whatever the size
+    (dict(d=256, **BIG), 2), (dict(d=80, **BIG), 2), (dict(d=256), 2),
+    # valid arguments, workspace larger than the static scratch: refused before any device access
+    (dict(**BIG), 2), (dict(dt=0, d=100, **BIG), 2),
+])
+def test_bwd_static_workspace_rejects_on_host(b, kw, code):
+    assert bwd_static(b, **kw) == code
+
+
 def km(b, ws=P, ws_bytes=1 << 30, dt=1, d=128, N=8, window=0, scale=0.1, o=P):
     vp = ctypes.c_void_p
     return b.lib.fa_fwd_key_major(vp(P), vp(P), vp(P), vp(o), vp(0), 1, 1, N, d, scale, window, dt, vp(ws), ws_bytes,

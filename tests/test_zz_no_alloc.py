@@ -55,3 +55,17 @@ def test_static_workspace_refuses_oversized_problems():
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd_static_workspace(x, x, x, x, lse, x, x, x, x)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+def test_static_workspace_binding_checks_lse():
+    """The wrapper rejects an lse of the wrong dtype, layout or size before
+    the library sees it (the kernels would read past a short one)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_tiled_attention_02_gb300 import binding as fa
+    dev = torch.device("cuda:0")
+    x = torch.zeros(1, 2, 256, 128, device=dev, dtype=torch.bfloat16)
+    good = torch.zeros(1, 2, 256, device=dev, dtype=torch.float32)
+    for bad in (good.half(), good[:, :1], torch.zeros(1, 256, 2, device=dev).transpose(1, 2)):
+        with pytest.raises(ValueError):
+            fa.fa_bwd_static_workspace(x, x, x, x, bad, x, x, x, x)
