@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = p.scale_log2;
     const int qlo = i0, qhi = i0 + BR - 1;
     float m_ref = -INFINITY;  // running reference maximum, log2 units of scaled scores
-    float l = 0.f;
+    float l = 0.f;            // row sum of the unrounded P (lse uses it)
+    float lc = 0.f;           // bf16 rounding error of each tile's largest P (O's normaliser adds it)
     bool ok = true;
     auto warp_wait = [&](uint32_t bar_addr, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
@@ -325,13 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 8; c < BC; c += 8)
 #pragma unroll
         for (int a = 0; a < 4; ++a) mx[a] = fmax3(mx[a], s[c + a], s[c + 4 + a]);
-      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl;
+      const float smax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      const float mt = smax * sl;
       float alpha = 1.f;
       if (mt > m_ref + kRescaleThreshold) {
         alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
         m_ref = mt;
       }
       const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      // The tile's largest P, computed exactly as its element is below.  P V
+      // multiplies bf16-rounded P while the row sum adds the unrounded
+      // values; where one key dominates a row, that key's rounding (up to
+      // 2^-9 of O: with lazy rescaling its P is 2^x, x in [0, 8]) is the whole
+      // mismatch, and adding it to O's normaliser cancels it.
+      const float pmax = ex2_approx(fmaf(smax, sl, nref));
+      lc = lc * alpha + (bf16_round(pmax) - pmax);
       const float2 sl2 = make_float2(sl, sl), nref2 = make_float2(nref, nref);
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // P (bf16 pairs) over the first 64 columns of the S buffer, in groups of
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool have = ok && ntiles > 0 && warp_wait(bar.drain(), 0);
     if (have) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / (l + lc);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

@@ -559,7 +559,9 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       const Item w = decode_item<WIN>(item, N, r);
       const int qi = w.i0 + t * BR + row;
       const int qlo = w.i0 + t * BR, qhi = qlo + BR - 1;
-      float m_ref = -INFINITY, l = 0.f;
+      // l: row sum of the unrounded P (lse uses it); lc: the bf16 rounding
+      // error of each tile's largest P, which O's normaliser adds (below)
+      float m_ref = -INFINITY, l = 0.f, lc = 0.f;
       for (int it = w.lo[t]; it < w.hi[t]; ++it, ++n) {
         if (!warp_wait(bar.s_full(t), n & 1)) {
           ok = false;
@@ -592,7 +594,8 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         for (int c = 8; c < BC; c += 8)
 #pragma unroll
           for (int a = 0; a < 4; ++a) mx[a] = fmax3(mx[a], s[c + a], s[c + 4 + a]);
-        const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl;
+        const float smax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        const float mt = smax * sl;
         float alpha = 1.f;
         if (mt > m_ref + kRescaleThreshold) {
           alpha = ex2_approx(m_ref - mt);
@@ -605,6 +608,15 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
           if (lane == 0) mbar_arrive(bar.alpha_ready(t));
         }
         const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        // The tile's largest P, computed exactly as its element is below
+        // (same fused multiply-add, same exp2).  P V multiplies the bf16
+        // rounding of every P, and the row sum adds the unrounded values; in
+        // a row that one key dominates (large logits) that mismatch is the
+        // dominant key's rounding, up to 2^-9 of O, because with lazy
+        // rescaling that P is 2^x, x in [0, 8], not exactly 1.  Adding the
+        // largest P's rounding error to O's normaliser cancels it.
+        const float pmax = ex2_approx(fmaf(smax, sl, nref));
+        lc = lc * alpha + (bf16_round(pmax) - pmax);
         const float2 sl2 = make_float2(sl, sl), nref2 = make_float2(nref, nref);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -678,7 +690,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
           break;
         }
         tc_fence_after();
-        const float inv_l = 1.f / l;
+        const float inv_l = 1.f / (l + lc);
         if constexpr (kStagedOut) {
           const uint32_t srow = sOst + row * (2 * C::DP);
 #pragma unroll

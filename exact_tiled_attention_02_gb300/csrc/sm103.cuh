@@ -73,6 +73,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// x rounded to the nearest bf16, as a float.
+__device__ __forceinline__ float bf16_round(float x) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x))) << 16);
+}
+
 // Register re-balancing between warpgroups (all 128 threads of a warpgroup
 // execute the same one).  The shares of all warpgroups must fit in the
 // registers the CTA was launched with.

@@ -1,10 +1,13 @@
 """GPU parity of the forward pass against the float64 oracle, through the C ABI.
 
-Tolerances: fp32 max-abs 1e-5; bf16 O max-abs 2e-2 and mean-abs 2e-3; lse
-(both dtypes) |diff| <= 1e-3 + 1e-5 |lse| for bf16, 1e-5 for fp32.  Small and
-medium shapes are compared element by element (several tiles and a ragged
-tail); the full-size workloads are compared on sampled rows that the oracle
-computes one by one, plus properties that hold at any size.
+Tolerances: fp32 max-abs 1e-5 on O and lse; bf16 O max-abs 2e-2 and
+mean-abs 2e-3, lse max-abs 1e-3.  Small and medium shapes are compared
+element by element (several tiles and a ragged tail), including shapes with
+more work items than the GPU has SMs, so that every CTA of the persistent
+kernels carries its barrier phases, K/V ring and (unmasked d = 128) its
+correction warps across items.  The full-size workloads are compared on whole
+heads, element by element, and on sampled rows of other heads, plus
+properties that hold at any size.
 """
 
 import numpy as np
@@ -40,7 +43,7 @@ def _check_bf16(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert err.mean() <= 2e-3, (what, err.mean())
     if lse_gpu is not None:
         le = np.abs(_np(lse_gpu) - lse_ref)
-        assert np.all(le <= 1e-3 + 1e-5 * np.abs(lse_ref)), (what, le.max())
+        assert le.max() <= 1e-3, (what, le.max())
 
 
 def test_workload1_f32_exact():
@@ -93,6 +96,19 @@ BF16_CASES = [
     # query tiles pass the d = 64 output staging tile back and forth; the last
     # item of every head has its second query tile wholly past N
     (1, 48, 1100, 64, 0, 1.0),
+    # the same at the other instantiations: 1100 rows make five items per
+    # head (the last one's second tile wholly past N), 400 items over 152
+    # CTAs.  Unmasked d = 128 runs the correction warpgroup; with Q, K x 8
+    # nearly every key tile moves some row's maximum, so the correction warps
+    # rescale O across item boundaries.
+    (1, 80, 1100, 128, 0, 8.0),
+    (1, 80, 1100, 128, 0, 1.0),
+    (2, 40, 1000, 128, 0, 8.0),
+    (1, 80, 1100, 128, 257, 1.0),
+    (1, 80, 1100, 128, 257, 8.0),
+    (1, 80, 1100, 96, 0, 1.0),
+    (1, 80, 1100, 96, 0, 8.0),
+    (1, 80, 1100, 64, 257, 1.0),
     (1, 1, 1, 96, 0, 1.0),
     (1, 2, 129, 96, 0, 1.0),
     (2, 1, 513, 96, 0, 8.0),
@@ -103,6 +119,9 @@ BF16_CASES = [
     (1, 1, 300, 256, 3, 1.0),
     (1, 2, 700, 256, 65, 1.0),
     (1, 1, 640, 256, 257, 8.0),
+    # d = 256 runs one 128-row query tile per CTA: 480 CTAs here
+    (1, 160, 300, 256, 0, 1.0),
+    (1, 160, 300, 256, 0, 8.0),
 ]
 
 
@@ -178,6 +197,39 @@ def test_full_size_workloads_sampled(index):
         o_ref, lse_ref = oracle.dense_forward_rows(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), w.scale, rows,
                                                    window=w.window)
         _check_bf16(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, (index, b, h))
+
+
+@pytest.mark.parametrize("index", [2, 3, 4, 5])
+def test_full_size_workloads_every_head(index):
+    """The full-size forward workloads, launched exactly as the bench launches
+    them (every CTA walks many work items), compared element by element with
+    the oracle on every row of every head: max-abs over the whole output and
+    mean-abs over the whole output.  The windowed workload uses the banded
+    oracle, which touches only in-band keys and is pinned to the dense
+    definition in the oracle's own tests.  (Sampled rows are not enough: at
+    Q, K x 8 the largest errors sit in rare rows where one key dominates.)"""
+    dev = _dev()
+    w = configs.WORKLOADS[index]
+    q, k, v = inputs.workload_inputs(w)
+    o, lse = _fa().fa_fwd(q.to(dev), k.to(dev), v.to(dev), scale=w.scale, window=w.window)
+    torch.cuda.synchronize()
+    assert _fa().fa_last_device_status() == 0
+    o_all, lse_all = o.float().cpu().numpy(), lse.cpu().numpy()
+    emax, esum, lmax = 0.0, 0.0, 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            qh, kh, vh = _np(q[b, h]), _np(k[b, h]), _np(v[b, h])
+            if w.window > 0:
+                o_ref, lse_ref = oracle.banded_forward_rows(qh, kh, vh, w.scale, np.arange(w.N), w.window)
+            else:
+                o_ref, lse_ref = oracle.dense_forward(qh, kh, vh, w.scale)
+            err = np.abs(o_all[b, h].astype(np.float64) - o_ref)
+            assert np.all(np.isfinite(err)), (index, b, h)
+            emax, esum = max(emax, float(err.max())), esum + float(err.sum())
+            lmax = max(lmax, float(np.abs(lse_all[b, h].astype(np.float64) - lse_ref).max()))
+    assert emax <= 2e-2, (index, emax)
+    assert esum / o_all.size <= 2e-3, (index, esum / o_all.size)
+    assert lmax <= 1e-3, (index, lmax)
 
 
 @pytest.mark.parametrize("d,window", [(96, 0), (96, 257), (256, 0), (256, 257)])

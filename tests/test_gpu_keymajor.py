@@ -1,6 +1,6 @@
 """GPU parity of the key-major forward schedule (the comparison schedule) against
 the float64 oracle, through the C ABI.  Same bars as the query-major bf16
-forward: O max-abs 2e-2 and mean-abs 2e-3; lse |diff| <= 1e-3 + 1e-5 |lse|."""
+forward: O max-abs 2e-2 and mean-abs 2e-3; lse max-abs 1e-3."""
 
 import numpy as np
 import pytest
@@ -34,7 +34,7 @@ def _check(o, lse, o_ref, lse_ref, what):
     assert err.max() <= 2e-2, (what, err.max())
     assert err.mean() <= 2e-3, (what, err.mean())
     le = np.abs(_np(lse) - lse_ref)
-    assert np.all(le <= 1e-3 + 1e-5 * np.abs(lse_ref)), (what, le.max())
+    assert le.max() <= 1e-3, (what, le.max())
 
 
 @pytest.mark.parametrize("B,H,N,d,window,qk", [
