@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--schedule", choices=["query-major", "key-major"], default="query-major",
                     help="forward loop order; key-major (outer loop over key tiles, O in device memory between "
                          "steps) is a comparison schedule and runs forward only")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-kernel timing of the other bf16 workloads (2, 4, 5) in the default line")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -369,6 +371,11 @@ def main():
                 "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(kernels[dom]["frac"], 4),
                 "traffic": traffic, "peak_source": peak_note}
 
+    workloads = None
+    default_line = args.shape is None and args.workload == 3 and not key_major and not args.no_bwd
+    if default_line and not args.no_workloads:
+        workloads = time_workloads(fa, (2, 4, 5), K, peaks, dev)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(fa, w, q, k, v, do, with_bwd, dev, K, pg, fwd_fn)
@@ -395,6 +402,7 @@ def main():
                        "l2": l2_note(w, qd)},
             "kernels": {n: {kk: round(vv, 4) for kk, vv in d.items()} for n, d in kernels.items()},
             "roofline": roofline,
+            "workloads": workloads,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": K * ((-(-w.N // 128) + 1) if key_major else 4 if tf32x3 else
@@ -405,6 +413,79 @@ def main():
     if pg is not None:
         pg.destroy_process_group()
     return 0
+
+
+def algorithmic_bytes(w, with_bwd: bool):
+    """HBM bytes the forward (and backward) must move at the least: the
+    forward reads Q, K, V and writes O and lse; the backward reads Q, K, V, O,
+    dO and lse and writes dQ, dK, dV."""
+    elt = 2 if w.dtype == "bf16" else 4
+    t = w.B * w.H * w.N * w.d * elt
+    rows = w.B * w.H * w.N * 4
+    fwd = 4 * t + rows
+    bwd = 8 * t + rows if with_bwd else 0
+    return fwd, bwd
+
+
+def time_workloads(fa, indices, steps, peaks, dev):
+    """Per-kernel times of other workloads of record, each on its own seeded
+    inputs, with CUDA events around each launch on the launching stream:
+    forward, then backward on the same batch.  Inputs smaller than L2 get an
+    L2 flush (a write of twice L2's size) before every step, outside the
+    timed launches.  Returns {workload name: {...}}."""
+    import torch
+
+    from exact_tiled_attention_02_gb300 import configs, inputs
+
+    out = {}
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    for idx in indices:
+        w = configs.WORKLOADS[idx]
+        q, k, v, do = (t.to(dev) for t in inputs.workload_inputs(w, with_do=True))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+        small = 4 * q.numel() * q.element_size() <= L2_BYTES
+
+        def one(evs=None):
+            if small:
+                flush.fill_(1)
+            if evs:
+                evs[0].record(stream)
+            fa.fa_fwd(q, k, v, scale=w.scale, window=w.window, o=o, lse=lse)
+            if evs:
+                evs[1].record(stream)
+            fa.fa_bwd(q, k, v, o, lse, do, scale=w.scale, window=w.window, dq=dq, dk=dk, dv=dv, workspace=ws)
+            if evs:
+                evs[2].record(stream)
+
+        for _ in range(3):
+            one()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            one(evs[i])
+        torch.cuda.synchronize()
+        assert fa.fa_last_device_status() == fa.FA_OK, f"a device-side wait timed out in workload {idx}"
+        fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        fb, bb = algorithmic_bytes(w, True)
+        rec = {}
+        for name, ms, fl, by in (("fwd", fwd_ms, w.fwd_flops(), fb), ("bwd", bwd_ms, w.bwd_flops(), bb)):
+            tf = fl / (ms * 1e-3) / 1e12
+            r = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4)}
+            if w.window > 0:
+                gbs = by / (ms * 1e-3) / 1e9
+                r.update({"hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
+            rec[name] = r
+        rec["config"] = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "window": w.window, "qk_mult": w.qk_mult,
+                         "l2": "flushed before every step" if small else "inputs larger than L2; no flush"}
+        out[w.name] = rec
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(fa, w, q, k, v, do, with_bwd, dev, steps, pg, fwd_fn=None):
