@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--no-bwd", action="store_true", help="forward only")
     ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16", help="dtype of a --shape problem")
     ap.add_argument("--f32-path", choices=["simt", "3xtf32"], default="simt",
-                    help="float32 forward: exact CUDA-core kernel, or the tensor-core 3xTF32 split (d <= 64, "
+                    help="float32 forward: exact CUDA-core kernel, or the tensor-core 3xTF32 split (d <= 128, "
                          "forward only)")
     ap.add_argument("--schedule", choices=["query-major", "key-major"], default="query-major",
                     help="forward loop order; key-major (outer loop over key tiles, O in device memory between "
@@ -405,7 +405,7 @@ def main():
             "workloads": workloads,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": K * ((-(-w.N // 128) + 1) if key_major else 4 if tf32x3 else
+            "gpu_launches": K * ((-(-w.N // 128) + 1) if key_major else (4 if w.d <= 64 else 3) if tf32x3 else
                                  (1 + (3 if with_bwd else 0))),
             "clocks": clocks,
         }

@@ -271,7 +271,7 @@ size_t fa_fwd_f32_3xtf32_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
   const long long bh = static_cast<long long>(B) * H;
   if (bh > 0x7fffffffLL) return 0;
-  return f32_tc_workspace_layout(static_cast<int>(bh), N, nullptr);
+  return f32_tc_workspace_layout(static_cast<int>(bh), N, d, nullptr);
 }
 
 fa_status fa_fwd_f32_3xtf32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
@@ -283,7 +283,6 @@ fa_status fa_fwd_f32_3xtf32(const float* q, const float* k, const float* v, floa
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID;
   const fa_status c = check_common(B, H, N, d, scale, window, FA_DTYPE_F32);
   if (c != FA_OK) return c;
-  if (d > 64) return FA_ERR_UNSUPPORTED;
   if (workspace_bytes < fa_fwd_f32_3xtf32_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
 
   FwdParams p{};

@@ -1,5 +1,7 @@
 // fwd_f32_tc_sm103.cu -- tiled exact attention forward for float32 inputs on
-// the tensor cores, by a three-term tf32 split ("3xTF32"), d <= 64.
+// the tensor cores, by a three-term tf32 split ("3xTF32"): the kernel for
+// d <= 64, the split kernels and the launcher for every d <= 128 (64 < d <=
+// 128 runs the kernel in fwd_f32_tc128_sm103.cu).
 //
 // What it computes is the forward of fwd_f32_simt.cu ("Flash attention and
 // efficient attention -- Hinglish notes", "The Standard Attention Problem",
@@ -15,8 +17,9 @@
 // float32 roundings of the exact value.
 //
 // Kernels:
-//   split_rows   Q and K -> hi / lo, [B*H][N][64] (columns past d zero)
-//   split_vt     V -> V^T hi / lo, [B*H][64][Npad] (Npad = N rounded up to 64),
+//   split_rows   Q and K -> hi / lo, [B*H][N][DP] (DP = 64, or 128 for d > 64;
+//                columns past d zero)
+//   split_vt     V -> V^T hi / lo, [B*H][DP][Npad] (Npad = N rounded up to 64),
 //                so that P V reads V K-major (keys contiguous), the layout
 //                tcgen05.mma takes for tf32 operands here
 //   main         one CTA = one 128-row query tile of one head, 192 threads:
@@ -80,11 +83,11 @@ struct Bars {
 };
 
 __global__ void __launch_bounds__(256) fa_split_rows_kernel(const float* __restrict__ x, float* __restrict__ hi,
-                                                            float* __restrict__ lo, long long rows, int d) {
+                                                            float* __restrict__ lo, long long rows, int d, int dp) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows * D) return;
-  const long long r = i / D;
-  const int c = static_cast<int>(i % D);
+  if (i >= rows * dp) return;
+  const long long r = i / dp;
+  const int c = static_cast<int>(i % dp);
   const float v = c < d ? x[r * d + c] : 0.f;
   const float h = tf32_rna(v);
   hi[i] = h;
@@ -92,11 +95,12 @@ __global__ void __launch_bounds__(256) fa_split_rows_kernel(const float* __restr
 }
 
 __global__ void __launch_bounds__(256) fa_split_vt_kernel(const float* __restrict__ v, float* __restrict__ hi,
-                                                          float* __restrict__ lo, long long BH, int N, int npad, int d) {
+                                                          float* __restrict__ lo, long long BH, int N, int npad, int d,
+                                                          int dp) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= BH * D * npad) return;
-  const long long bh = i / (static_cast<long long>(D) * npad);
-  const long long rem = i % (static_cast<long long>(D) * npad);
+  if (i >= BH * dp * npad) return;
+  const long long bh = i / (static_cast<long long>(dp) * npad);
+  const long long rem = i % (static_cast<long long>(dp) * npad);
   const int c = static_cast<int>(rem / npad), n = static_cast<int>(rem % npad);
   const float x = (c < d && n < N) ? v[(bh * N + n) * d + c] : 0.f;
   const float h = tf32_rna(x);
@@ -436,39 +440,53 @@ cudaError_t launch_main(const FwdParams& p, const TcMaps& m, cudaStream_t s) {
 
 }  // namespace
 
-size_t f32_tc_workspace_layout(int BH, int N, size_t off[6]) {
+size_t f32_tc_workspace_layout(int BH, int N, int d, size_t off[6]) {
+  const size_t dp = d <= D ? D : 128;
   const size_t npad = (static_cast<size_t>(N) + 63) & ~size_t(63);
-  const size_t rows = (static_cast<size_t>(BH) * N * D * 4 + 255) & ~size_t(255);
-  const size_t vt = (static_cast<size_t>(BH) * D * npad * 4 + 255) & ~size_t(255);
+  const size_t rows = (static_cast<size_t>(BH) * N * dp * 4 + 255) & ~size_t(255);
+  const size_t vt = (static_cast<size_t>(BH) * dp * npad * 4 + 255) & ~size_t(255);
   size_t o = 0;
-  for (int i = 0; i < 4; ++i, o += rows)
+  for (int i = 0; i < 4; ++i) {
     if (off) off[i] = o;
+    if (i >= 2 || d <= D) o += rows;  // Q hi / lo only for d <= 64
+  }
   for (int i = 4; i < 6; ++i, o += vt)
     if (off) off[i] = o;
   return o;
 }
 
 cudaError_t launch_fwd_f32_tc(const FwdParams& p, void* workspace, EncodeTiledFnPtr encode, cudaStream_t s) {
-  if (p.d > D || encode == nullptr) return cudaErrorInvalidValue;
+  if (p.d > 128 || encode == nullptr) return cudaErrorInvalidValue;
+  const int dp = p.d <= D ? D : 128;
   size_t off[6];
-  f32_tc_workspace_layout(p.BH, p.N, off);
+  f32_tc_workspace_layout(p.BH, p.N, p.d, off);
   char* ws = static_cast<char*>(workspace);
   float* buf[6];
   for (int i = 0; i < 6; ++i) buf[i] = reinterpret_cast<float*>(ws + off[i]);
   const long long rows = static_cast<long long>(p.BH) * p.N;
   const int npad = (p.N + 63) & ~63;
-  const long long n1 = rows * D, n2 = static_cast<long long>(p.BH) * D * npad;
+  const long long n1 = rows * dp, n2 = static_cast<long long>(p.BH) * dp * npad;
   if ((n1 + 255) / 256 > 0x7fffffffLL || (n2 + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_split_rows_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.q), buf[0],
-                                                                                buf[1], rows, p.d);
+  if (dp == D)
+    fa_split_rows_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.q),
+                                                                                  buf[0], buf[1], rows, p.d, dp);
   fa_split_rows_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.k), buf[2],
-                                                                                buf[3], rows, p.d);
+                                                                                buf[3], rows, p.d, dp);
   fa_split_vt_kernel<<<static_cast<unsigned>((n2 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.v), buf[4],
-                                                                              buf[5], p.BH, p.N, npad, p.d);
+                                                                              buf[5], p.BH, p.N, npad, p.d, dp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  TcMaps m;
   const uint64_t BH = static_cast<uint64_t>(p.BH), Nn = static_cast<uint64_t>(p.N);
+  if (dp != D) {
+    Tc128Maps m;
+    if (!make_map_f32(&m.kh, encode, buf[2], 128, Nn, BH, 32, 64) ||
+        !make_map_f32(&m.kl, encode, buf[3], 128, Nn, BH, 32, 64) ||
+        !make_map_f32(&m.vh, encode, buf[4], static_cast<uint64_t>(npad), 128, BH, 32, 128) ||
+        !make_map_f32(&m.vl, encode, buf[5], static_cast<uint64_t>(npad), 128, BH, 32, 128))
+      return cudaErrorInvalidValue;
+    return launch_fwd_f32_tc128_main(p, m, s);
+  }
+  TcMaps m;
   if (!make_map_f32(&m.qh, encode, buf[0], D, Nn, BH, 32, BR) || !make_map_f32(&m.ql, encode, buf[1], D, Nn, BH, 32, BR) ||
       !make_map_f32(&m.kh, encode, buf[2], D, Nn, BH, 32, BC) || !make_map_f32(&m.kl, encode, buf[3], D, Nn, BH, 32, BC) ||
       !make_map_f32(&m.vh, encode, buf[4], static_cast<uint64_t>(npad), D, BH, 32, D) ||

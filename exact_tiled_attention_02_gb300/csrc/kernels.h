@@ -84,12 +84,21 @@ cudaError_t launch_fwd_bf16_d256(const FwdParams& p, const FwdMaps& m, cudaStrea
 typedef CUresult (*EncodeTiledFnPtr)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-// fp32 forward on the tensor cores by the 3xTF32 split (d <= 64): workspace =
-// Q hi, Q lo, K hi, K lo as [BH][N][64] fp32, then V^T hi, V^T lo as
-// [BH][64][Npad] fp32 (Npad = N rounded up to 64), each 256-byte aligned;
-// off (may be null) receives the six section offsets.
-size_t f32_tc_workspace_layout(int BH, int N, size_t off[6]);
+// fp32 forward on the tensor cores by the 3xTF32 split (d <= 128): workspace =
+// Q hi, Q lo, K hi, K lo as [BH][N][DP] fp32, then V^T hi, V^T lo as
+// [BH][DP][Npad] fp32 (DP = 64 for d <= 64, else 128; Npad = N rounded up
+// to 64), each 256-byte aligned.  For d > 64 the Q sections are empty (that
+// kernel splits Q itself, into tensor memory).  off (may be null) receives
+// the six section offsets.
+size_t f32_tc_workspace_layout(int BH, int N, int d, size_t off[6]);
 cudaError_t launch_fwd_f32_tc(const FwdParams& p, void* workspace, EncodeTiledFnPtr encode, cudaStream_t s);
+// 64 < d <= 128 (fwd_f32_tc128_sm103.cu): maps over K hi / lo ([BH][N][128],
+// box (32, 64, 1)) and V^T hi / lo ([BH][128][Npad], box (32, 128, 1)), fp32,
+// 128-byte swizzle.
+struct Tc128Maps {
+  CUtensorMap kh, kl, vh, vl;
+};
+cudaError_t launch_fwd_f32_tc128_main(const FwdParams& p, const Tc128Maps& m, cudaStream_t s);
 // Key-major forward (comparison schedule): one launch per key tile, then a
 // finishing launch; workspace = fp32 O~ [BH,N,d], then m and l [BH,N], each
 // section 256-byte aligned.

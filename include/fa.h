@@ -118,7 +118,7 @@ size_t fa_fwd_key_major_workspace_bytes(int B, int H, int N, int d);
 /*
  * The float32 forward on the tensor cores.  Same operation, layouts, window
  * and results as fa_fwd with FA_DTYPE_F32 (q, k, v, o float32 [B,H,N,d], lse
- * float32 [B,H,N] or NULL), for 1 <= d <= 64.  The tensor cores multiply
+ * float32 [B,H,N] or NULL), for 1 <= d <= 128.  The tensor cores multiply
  * tf32 values (11 significant bits), so every float32 operand x is split as
  * hi = tf32(x), lo = tf32(x - hi) and each product is taken as
  * hi*hi + hi*lo + lo*hi (the "3xTF32" scheme): S = Q K^T from split Q and K,
@@ -128,10 +128,12 @@ size_t fa_fwd_key_major_workspace_bytes(int B, int H, int N, int d);
  * little of that accuracy for tensor-core speed.
  *   workspace        at least fa_fwd_f32_3xtf32_workspace_bytes() bytes,
  *                    256-byte aligned, owned by the caller (it receives the
- *                    split copies of Q, K and V: 6 x 4 x B*H*N*64 bytes, N
+ *                    split copies of Q, K and V: 6 x 4 x B*H*N*64 bytes for
+ *                    d <= 64; for 64 < d <= 128 those of K and V only, 4 x 4
+ *                    x B*H*N*128 bytes, the kernel splitting Q itself; N
  *                    rounded up to 64 for V); contents on entry do not
  *                    matter and are undefined on return.
- * d > 64 returns FA_ERR_UNSUPPORTED; other arguments and errors as fa_fwd.
+ * d > 128 returns FA_ERR_UNSUPPORTED; other arguments and errors as fa_fwd.
  */
 fa_status fa_fwd_f32_3xtf32(const float* q, const float* k, const float* v, float* o, float* lse,
                             int B, int H, int N, int d, float scale, int window,

@@ -152,8 +152,8 @@ def tf(b, ws=P, ws_bytes=1 << 30, d=64, N=8, window=0, scale=0.1, o=P, lse=0):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=0), 1), (dict(ws=P + 16), 1), (dict(ws_bytes=100), 1), (dict(o=0), 1), (dict(o=P + 4), 1),
-    (dict(lse=P + 2), 1), (dict(window=2), 1), (dict(scale=0.0), 1), (dict(N=0), 1), (dict(d=65), 2),
-    (dict(d=128), 2),
+    (dict(lse=P + 2), 1), (dict(window=2), 1), (dict(scale=0.0), 1), (dict(N=0), 1), (dict(d=129), 2),
+    (dict(d=256), 2),
 ])
 def test_3xtf32_rejects_on_host(b, kw, code):
     assert tf(b, **kw) == code
@@ -165,6 +165,10 @@ def test_3xtf32_workspace_size(b):
     rows = (2 * 100 * 64 * 4 + 255) // 256 * 256
     vt = 2 * 64 * 128 * 4
     assert b.fa_fwd_f32_3xtf32_workspace_bytes(2, 1, 100, 16) == 4 * rows + 2 * vt
+    # 64 < d <= 128: K hi/lo rows of 128 and V^T hi/lo with 128 rows; Q is split in the kernel
+    rows = (2 * 100 * 128 * 4 + 255) // 256 * 256
+    vt = 2 * 128 * 128 * 4
+    assert b.fa_fwd_f32_3xtf32_workspace_bytes(2, 1, 100, 100) == 2 * rows + 2 * vt
 
 
 def test_selftest_rejects_bad_limit(b):
