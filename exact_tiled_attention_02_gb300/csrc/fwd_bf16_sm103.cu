@@ -183,10 +183,30 @@ struct Item {
   int lo[2], hi[2];
 };
 
+// Items [0, n_pair) are pairs of query tiles.  Unmasked, when the last round
+// of pairs would fill at most half the CTAs, the launcher passes n_pair
+// smaller than the number of pairs and the remaining pairs run as single
+// query tiles, items n_pair, n_pair + 1, ... (item n_pair + s holds tile s % 2
+// of pair n_pair + s / 2; its second tile is empty), so that they spread over
+// twice as many CTAs.
 template <bool WIN>
-__device__ __forceinline__ Item decode_item(int item, int N, int r) {
+__device__ __forceinline__ Item decode_item(int item, int N, int r, int n_pair) {
   Item w;
   const int nqt = (N + 2 * BR - 1) / (2 * BR);
+  if (!WIN && item >= n_pair) {
+    const int s = item - n_pair, pair = n_pair + s / 2;
+    w.bh = pair / nqt;
+    w.i0 = (pair % nqt) * (2 * BR) + (s & 1) * BR;
+    w.j_lo = 0;
+    // a tile wholly past N (the second tile of a head's last pair) makes an
+    // empty item: no key tiles, so no role loads or waits for any
+    w.ntiles = w.i0 < N ? (N + BC - 1) / BC : 0;
+    w.lo[0] = 0;
+    w.hi[0] = w.ntiles;
+    w.lo[1] = 0;
+    w.hi[1] = 0;
+    return w;
+  }
   w.bh = item / nqt;
   w.i0 = (item % nqt) * (2 * BR);
   w.j_lo = 0;
@@ -215,7 +235,8 @@ __device__ __forceinline__ Item decode_item(int item, int N, int r) {
 template <int D, bool WIN>
 __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
     fa_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                                     const __grid_constant__ CUtensorMap tmv, const FwdParams p, int n_items) {
+                                     const __grid_constant__ CUtensorMap tmv, const FwdParams p, int n_items,
+                                     int n_pair) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -288,7 +309,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       int nt[2] = {0, 0};  // key tiles each query tile has passed (all items)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const Item w = decode_item<WIN>(item, N, r);
+        const Item w = decode_item<WIN>(item, N, r, n_pair);
         for (int it = 0; ok && it < w.ntiles; ++it) {
           for (int t = 0; t < 2; ++t) {
             if (it < w.lo[t] || it >= w.hi[t]) continue;
@@ -339,7 +360,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       int g = 0;         // ring slots issued so far (all items)
       int nq = 0;        // items whose Q was issued
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++nq) {
-        const Item w = decode_item<WIN>(item, N, r);
+        const Item w = decode_item<WIN>(item, N, r, n_pair);
         for (int t = 0; t < 2; ++t) {
           // the previous item's last Q_t K^T has completed
           if (nq > 0 && !mbar_wait_backoff(bar.q_empty(t), (nq - 1) & 1, wc)) {
@@ -432,7 +453,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       };
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++nq) {
-        const Item w = decode_item<WIN>(item, N, r);
+        const Item w = decode_item<WIN>(item, N, r, n_pair);
         ok = mbar_wait2(bar.q_full(0), nq & 1, bar.q_full(1), nq & 1, wc);
         if (!ok) break;
         tc_fence_after();
@@ -440,7 +461,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
           last[t] = w.hi[t] - 1;
           if (w.lo[t] >= w.hi[t]) mma_commit(bar.q_empty(t));  // no product reads Q_t in this item
         }
-        if (!WIN) {
+        if (!WIN && w.lo[1] < w.hi[1]) {
           // both tiles take every key tile: PV0(j), S0(j+1), PV1(j), release, S1(j+1)
           ok = wait_k(0);
           if (ok) {
@@ -488,7 +509,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
           cnt[0] += w.ntiles;
           cnt[1] += w.ntiles;
         } else {
-          // windowed: each tile only over its own key range
+          // windowed, or a single-tile item: each tile only over its own key range
           for (int t = 0; t < 2; ++t) {
             if (!ok || w.lo[t] >= w.hi[t]) continue;
             ok = wait_k(w.lo[t]);
@@ -556,7 +577,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
     };
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const Item w = decode_item<WIN>(item, N, r);
+      const Item w = decode_item<WIN>(item, N, r, n_pair);
       const int qi = w.i0 + t * BR + row;
       const int qlo = w.i0 + t * BR, qhi = qlo + BR - 1;
       // l: row sum of the unrounded P (lse uses it); lc: the bf16 rounding
@@ -809,13 +830,21 @@ cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const long long items = static_cast<long long>((p.N + 2 * BR - 1) / (2 * BR)) * p.BH;
-  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long pairs = static_cast<long long>((p.N + 2 * BR - 1) / (2 * BR)) * p.BH;
+  if (2 * pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid = static_cast<int>(items < sms ? items : sms);
-  fa_fwd_bf16_sm103_kernel<D, WIN><<<grid, threads_for<D, WIN>(), C::SMEM_BYTES, s>>>(m.q, m.k, m.v, p,
-                                                                                 static_cast<int>(items));
+  const int grid = static_cast<int>(pairs < sms ? pairs : sms);
+  // Unmasked: a last round of pairs that fills at most half the CTAs runs as
+  // single query tiles instead (twice the items, each half the work).
+  long long n_pair = pairs, items = pairs;
+  const long long rem = pairs % grid;
+  if (!WIN && p.N > BR && rem > 0 && 2 * rem <= grid) {
+    n_pair = pairs - rem;
+    items = n_pair + 2 * rem;
+  }
+  fa_fwd_bf16_sm103_kernel<D, WIN><<<grid, threads_for<D, WIN>(), C::SMEM_BYTES, s>>>(
+      m.q, m.k, m.v, p, static_cast<int>(items), static_cast<int>(n_pair));
   return cudaGetLastError();
 }
 
@@ -823,6 +852,9 @@ cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
 
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
   const bool win = p.window_r >= 0;
+  // narrow bands (at most three key tiles per query tile): one query tile per
+  // CTA, two CTAs per SM (fwd_bf16_win_sm103.cu)
+  if (win && p.d != 256 && p.window_r <= 128) return launch_fwd_bf16_win(p, m, s);
   if (p.d == 128) return win ? launch_d<128, true>(p, m, s) : launch_d<128, false>(p, m, s);
   if (p.d == 64) return win ? launch_d<64, true>(p, m, s) : launch_d<64, false>(p, m, s);
   if (p.d == 96) return win ? launch_d<96, true>(p, m, s) : launch_d<96, false>(p, m, s);

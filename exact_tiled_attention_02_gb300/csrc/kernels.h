@@ -80,6 +80,9 @@ struct BwdMaps {
 cudaError_t launch_fwd_f32_simt(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16_tc(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d256(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
+// Windowed forward at d = 64, 96, 128 for bands of radius <= 128: one
+// 128-row query tile per CTA, two CTAs per SM (fwd_bf16_win_sm103.cu).
+cudaError_t launch_fwd_bf16_win(const FwdParams& p, const FwdMaps& m, cudaStream_t s);
 // cuTensorMapEncodeTiled's signature (resolved at run time by the C-ABI layer)
 typedef CUresult (*EncodeTiledFnPtr)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

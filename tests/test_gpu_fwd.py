@@ -109,6 +109,17 @@ BF16_CASES = [
     (1, 80, 1100, 96, 0, 1.0),
     (1, 80, 1100, 96, 0, 8.0),
     (1, 80, 1100, 64, 257, 1.0),
+    # 200 pairs of query tiles on 152 CTAs: the last 48 pairs run as 96
+    # single query tiles (the last pair of every head has its second tile
+    # wholly past N, so one of its two single items is empty)
+    (1, 40, 1100, 128, 0, 8.0),
+    (1, 40, 1100, 96, 0, 1.0),
+    (1, 40, 1100, 64, 0, 1.0),
+    # bands wider than radius 128 run the two-tile persistent kernel; narrower
+    # ones one query tile per CTA
+    (1, 80, 1100, 128, 1025, 1.0),
+    (1, 40, 1500, 96, 513, 8.0),
+    (1, 40, 1500, 64, 259, 1.0),
     (1, 1, 1, 96, 0, 1.0),
     (1, 2, 129, 96, 0, 1.0),
     (2, 1, 513, 96, 0, 8.0),
