@@ -12,8 +12,10 @@
 // With a narrow band a query tile meets few key tiles (three for r = 128),
 // so a CTA that pairs two query tiles spends much of each item filling and
 // draining its pipeline: measured, the first tile's softmax idled about half
-// of every item.  The launcher uses this kernel for r <= 128 (at most three
-// key tiles per query tile); wider bands keep the two-tile persistent kernel,
+// of every item.  Here each CTA holds one query tile at a time, and two
+// persistent CTAs per SM walk the query tiles; the launcher uses this kernel
+// for r <= 128 (at most three key tiles per query tile); wider bands keep the
+// two-tile persistent kernel,
 // whose two-stage K/V ring hides the loads of long key loops (measured at
 // 1 x 32 x 16384: w = 65, d = 128: 0.162 against 0.167 ms; w = 257: d = 64
 // 0.126 against 0.138, d = 96 0.139 against 0.143, d = 128 0.151 both;
@@ -58,8 +60,8 @@ struct CfgW {
   static constexpr int BOXES = DP / 64;
   static constexpr int TILE = BOXES * BOX_BYTES;
   static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE, OFF_BAR = 3 * TILE;
-  // q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, drain
-  static constexpr int NBAR = 9;
+  // q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, drain, q_empty
+  static constexpr int NBAR = 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // at least 80 KB, so that no more than two CTAs share an SM: tensor memory
@@ -80,12 +82,13 @@ struct Bars {
   __device__ uint32_t p_full() const { return base + 48; }
   __device__ uint32_t o_done() const { return base + 56; }
   __device__ uint32_t drain() const { return base + 64; }
+  __device__ uint32_t q_empty() const { return base + 72; }
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_bf16_win_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                                 const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
+                                 const __grid_constant__ CUtensorMap tmv, const FwdParams p, int n_tiles) {
   using C = CfgW<D>;
   constexpr int DP = C::DP, TILE = C::TILE;
   extern __shared__ uint8_t smem_raw[];
@@ -106,12 +109,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N, r = p.window_r;
   const int nqt = (N + BR - 1) / BR;
-  const int bh = blockIdx.x / nqt;
-  const int i0 = (blockIdx.x % nqt) * BR;
-  // the key tiles that meet this query tile's band
-  const int j_lo = max(0, i0 - r) / BC;
-  const int j_hi = (min(N, min(N, i0 + BR) + r) + BC - 1) / BC;
-  const int ntiles = j_hi - j_lo;
+  // query tile t of the CTA's list: its head, first row, and the key tiles
+  // that meet its band
+  struct Tile {
+    int bh, i0, j_lo, ntiles;
+  };
+  auto tile_of = [&](int t) {
+    Tile w;
+    w.bh = t / nqt;
+    w.i0 = (t % nqt) * BR;
+    w.j_lo = max(0, w.i0 - r) / BC;
+    w.ntiles = (min(N, min(N, w.i0 + BR) + r) + BC - 1) / BC - w.j_lo;
+    return w;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar.q_full(), 1);
@@ -123,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(bar.p_full(), 4);  // one arrive per softmax warp
     mbar_init(bar.o_done(), 1);
     mbar_init(bar.drain(), 1);
+    mbar_init(bar.q_empty(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -142,33 +153,43 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch_tensormap(&tmq);
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
-      mbar_arrive_expect_tx(bar.q_full(), TILE);
-      for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sQ + b * BOX_BYTES, &tmq, bar.q_full(), b * 64, i0, bh);
       bool ok = true;
-      int kq = 0, vq = 0;  // K / V tiles issued
-      // consumption order S_0, P_0 V_0, S_1, P_1 V_1, ...: K_j loads once S_{j-1}
-      // has read K_{j-1}, V_j once P_{j-1} V_{j-1} has read V_{j-1}
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int kv0 = (j_lo + j) * BC;
-        if (j > 0 && !mbar_wait_backoff(bar.k_empty(), (j - 1) & 1, wc)) {
+      int g = 0, nt = 0;   // key tiles and query tiles of this CTA's list reached
+      int kq = 0, vq = 0;  // K and V loads issued
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++nt) {
+        const Tile w = tile_of(t);
+        // Q once the previous tile's last S has read the old one
+        if (nt > 0 && !mbar_wait_backoff(bar.q_empty(), (nt - 1) & 1, wc)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar.k_full(), TILE);
-        for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sK + b * BOX_BYTES, &tmk, bar.k_full(), b * 64, kv0, bh);
-        kq = j + 1;
-        if (j > 0 && !mbar_wait_backoff(bar.v_empty(), (j - 1) & 1, wc)) {
-          ok = false;
-          break;
+        mbar_arrive_expect_tx(bar.q_full(), TILE);
+        for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sQ + b * BOX_BYTES, &tmq, bar.q_full(), b * 64, w.i0, w.bh);
+        // consumption order S_0, P_0 V_0, S_1, P_1 V_1, ... (across tiles): K
+        // loads once the previous S has read K, V once the previous P V has
+        // read V
+        for (int j = 0; ok && j < w.ntiles; ++j, ++g) {
+          const int kv0 = (w.j_lo + j) * BC;
+          if (g > 0 && !mbar_wait_backoff(bar.k_empty(), (g - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar.k_full(), TILE);
+          for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sK + b * BOX_BYTES, &tmk, bar.k_full(), b * 64, kv0, w.bh);
+          ++kq;
+          if (g > 0 && !mbar_wait_backoff(bar.v_empty(), (g - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar.v_full(), TILE);
+          for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sV + b * BOX_BYTES, &tmv, bar.v_full(), b * 64, kv0, w.bh);
+          ++vq;
         }
-        mbar_arrive_expect_tx(bar.v_full(), TILE);
-        for (int b = 0; b < C::BOXES; ++b) tma_load_3d(sV + b * BOX_BYTES, &tmv, bar.v_full(), b * 64, kv0, bh);
-        vq = j + 1;
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory is released
         WaitCtl drain{nullptr, nullptr, wc.limit_ns};
-        mbar_wait(bar.q_full(), 0, drain);
+        if (nt > 0) mbar_wait(bar.q_full(), (nt - 1) & 1, drain);
         if (kq > 0) mbar_wait(bar.k_full(), (kq - 1) & 1, drain);
         if (vq > 0) mbar_wait(bar.v_full(), (vq - 1) & 1, drain);
       }
@@ -179,27 +200,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BR, BC, 0, 0);  // Q, K: K-major
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, DP, 0, 1);  // P (TMEM), V: MN-major
-      bool ok = mbar_wait(bar.q_full(), 0, wc);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        // S_j = Q K_j^T (over P_{j-1}, which P_{j-1} V_{j-1}, issued before, has read)
-        if (!mbar_wait(bar.k_full(), j & 1, wc)) break;
-        tc_fence_after();
+      bool ok = true;
+      int g = 0, nt = 0;  // key tiles and query tiles consumed
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++nt) {
+        const Tile w = tile_of(t);
+        if (!mbar_wait(bar.q_full(), nt & 1, wc)) break;
+        for (int j = 0; j < w.ntiles; ++j, ++g) {
+          // S_j = Q K_j^T (over P_{j-1}, which P_{j-1} V_{j-1}, issued before, has read)
+          if (!mbar_wait(bar.k_full(), g & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          mma_bf16_ss(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idesc_qk, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+            mma_bf16_ss(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idesc_qk, kk > 0);
+          }
+          mma_commit(bar.k_empty());
+          if (j + 1 == w.ntiles) mma_commit(bar.q_empty());  // the tile's last reader of Q
+          mma_commit(bar.s_full());
+          // O (+)= P_j V_j.  The first P of a tile also means the softmax warps
+          // have read the previous tile's O out of tensor memory.
+          if (!mbar_wait2(bar.p_full(), g & 1, bar.v_full(), g & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BC / 16; ++kk)
+            mma_bf16_ts(tmem + kTmemO, tmem + kk * 8, sdesc_sw128(sV + kk * 16 * 128, BOX_BYTES, 1024), idesc_pv,
+                        (j > 0 || kk > 0));
+          mma_commit(bar.v_empty());
+          mma_commit(bar.o_done());
         }
-        mma_commit(bar.k_empty());
-        mma_commit(bar.s_full());
-        // O (+)= P_j V_j
-        if (!mbar_wait2(bar.p_full(), j & 1, bar.v_full(), j & 1, wc)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ts(tmem + kTmemO, tmem + kk * 8, sdesc_sw128(sV + kk * 16 * 128, BOX_BYTES, 1024), idesc_pv,
-                      (j > 0 || kk > 0));
-        mma_commit(bar.v_empty());
-        mma_commit(bar.o_done());
       }
       // every MMA this thread issued must finish before tensor memory is freed
       mma_commit(bar.drain());
@@ -210,20 +244,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     // -------------------------------------------------------------- softmax
     const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int qi = i0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const uint32_t tO = tl + kTmemO;
     const float sl = p.scale_log2;
-    const int qlo = i0, qhi = i0 + BR - 1;
-    float m_ref = -INFINITY;  // running reference maximum, log2 units of scaled scores
-    float l = 0.f;            // row sum of the unrounded P (lse uses it)
-    float lc = 0.f;           // bf16 rounding error of each tile's largest P (O's normaliser adds it)
     bool ok = true;
     auto warp_wait = [&](uint32_t bar_addr, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
     };
-    for (int j = 0; j < ntiles; ++j) {
-      if (!warp_wait(bar.s_full(), j & 1)) {
+    int g = 0;  // key tiles processed (all of this CTA's tiles)
+    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+    const Tile w = tile_of(t);
+    const int bh = w.bh, i0 = w.i0, j_lo = w.j_lo, ntiles = w.ntiles;
+    const int qi = i0 + row;
+    const int qlo = i0, qhi = i0 + BR - 1;
+    float m_ref = -INFINITY;  // running reference maximum, log2 units of scaled scores
+    float l = 0.f;            // row sum of the unrounded P (lse uses it)
+    float lc = 0.f;           // bf16 rounding error of each tile's largest P (O's normaliser adds it)
+    for (int j = 0; j < ntiles; ++j, ++g) {
+      if (!warp_wait(bar.s_full(), g & 1)) {
         ok = false;
         break;
       }
@@ -312,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the last P V has completed once o_done's last phase has; each thread
     // stores its own row of O with 16-byte stores (staging the tile in Q's
     // free buffer for whole-row warp stores measured 2-3% slower here)
-    const bool have = ok && ntiles > 0 && warp_wait(bar.o_done(), (ntiles - 1) & 1);
+    const bool have = ok && ntiles > 0 && warp_wait(bar.o_done(), (g - 1) & 1);
     if (have) {
       tc_fence_after();
       const float inv_l = 1.f / (l + lc);
@@ -339,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         p.lse[static_cast<size_t>(bh) * N + qi] = (mref + __log2f(l)) * 0.69314718055994531f;
       }
     }
+    }  // tiles
   }
 
   tc_fence_before();
@@ -359,9 +398,16 @@ cudaError_t launch_d(const FwdParams& p, const FwdMaps& m, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const long long grid = static_cast<long long>((p.N + BR - 1) / BR) * p.BH;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_fwd_bf16_win_sm103_kernel<D><<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(m.q, m.k, m.v, p);
+  const long long tiles = static_cast<long long>((p.N + BR - 1) / BR) * p.BH;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    return cudaErrorInvalidDevice;
+  // persistent: two CTAs per SM walk the query tiles
+  const long long grid = tiles < 2LL * sms ? tiles : 2LL * sms;
+  fa_fwd_bf16_win_sm103_kernel<D><<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, s>>>(
+      m.q, m.k, m.v, p, static_cast<int>(tiles));
   return cudaGetLastError();
 }
 
