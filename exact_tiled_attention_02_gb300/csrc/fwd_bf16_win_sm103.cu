@@ -59,7 +59,9 @@ struct CfgW {
   static constexpr int DP = (D + 63) / 64 * 64;
   static constexpr int BOXES = DP / 64;
   static constexpr int TILE = BOXES * BOX_BYTES;
-  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE, OFF_BAR = 3 * TILE;
+  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE;
+  static constexpr int OFF_OST = 3 * TILE;  // per softmax warp: 32 rows x 64 bytes of O (2 KB)
+  static constexpr int OFF_BAR = OFF_OST + 4 * 2048;
   // q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, drain, q_empty
   static constexpr int NBAR = 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (u32) + abort flag (int)
@@ -347,28 +349,44 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ------------------------------------------------------------ epilogue
-    // the last P V has completed once o_done's last phase has; each thread
-    // stores its own row of O with 16-byte stores (staging the tile in Q's
-    // free buffer for whole-row warp stores measured 2-3% slower here)
+    // The last P V has completed once o_done's last phase has.  Each warp
+    // writes its 32 rows of O 32 columns (64 bytes a row) at a time through a
+    // 2 KB staging buffer of its own: every thread puts its row's 64 bytes
+    // there (16-byte chunk q of row r at position q ^ (r / 2 % 4), so that a
+    // chunk of the 32 rows covers all eight 16-byte bank groups of a 128-byte
+    // span), then the warp stores whole
+    // 64-byte row segments, 8 rows per instruction (from registers, one row
+    // per thread, each instruction touched 32 rows in 16-byte pieces).
     const bool have = ok && ntiles > 0 && warp_wait(bar.o_done(), (g - 1) & 1);
     if (have) {
       tc_fence_after();
       const float inv_l = 1.f / (l + lc);
-      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * N + qi) * D * 2;
+      const uint32_t ost = sb + C::OFF_OST + (warp & 3) * 2048;
+      const int r32 = lane;  // this thread's row within the warp's 32
+      const int rbase = i0 + (warp & 3) * 32;
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * N + rbase) * D * 2;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tO + c * 32, o);
         tmem_wait_ld();
-        if (qi < N && !*abort_flag) {
+        __syncwarp();  // the previous chunk's stores have read the buffer
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-            st_global_v4(orow + (c * 4 + q4) * 16, v);
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(ost + r32 * 64 + ((q4 ^ ((r32 >> 1) & 3)) << 4),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l));
+        __syncwarp();
+        if (!*abort_flag) {
+#pragma unroll
+          for (int piece = 0; piece < 4; ++piece) {
+            const int idx = piece * 32 + lane;  // 128 pieces of 16 bytes: row idx / 4, chunk idx % 4
+            const int rr = idx >> 2, q4 = idx & 3;
+            if (rbase + rr < N)
+              st_global_v4(obase + static_cast<size_t>(rr) * D * 2 + c * 64 + q4 * 16,
+                           ld_shared_v4(ost + rr * 64 + ((q4 ^ ((rr >> 1) & 3)) << 4)));
           }
         }
       }
