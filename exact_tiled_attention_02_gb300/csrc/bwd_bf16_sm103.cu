@@ -145,7 +145,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                             const __grid_constant__ CUtensorMap tmdq, const BwdParams p) {
+                             const __grid_constant__ CUtensorMap tmdq, const __grid_constant__ CUtensorMap tmdk,
+                             const __grid_constant__ CUtensorMap tmdv, const BwdParams p) {
   using C = Cfg<D>;
   constexpr int STAGES = C::STAGES;
   constexpr int TILE_BYTES = C::TILE_BYTES, STAGE_BYTES = C::STAGE_BYTES;
@@ -552,6 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (have) {
+      // staged in the TMA box layout of the outputs' maps ([128 keys][64
+      // columns] boxes, 16-byte chunk c of row r at c ^ (r % 8)), then written
+      // by two TMA stores per warpgroup; keys past N are not written (from
+      // registers, a thread per row: ≈ 4000 cycles per 128 keys at the
+      // window-257 workload)
       tc_fence_after();
       const uint32_t tcol = g == 0 ? TM_DV : TM_DK;
       const float mul = g == 0 ? 1.f : p.scale;
@@ -567,22 +573,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * mul, __uint_as_float(v[q4 * 8 + 2 * e + 1]) * mul);
-          // row-major [128 keys][DP] bf16 with 16-byte chunks swizzled by row
-          st_shared_v4(stage_out + row * (2 * C::DP) + ((c16 ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+          st_shared_v4(stage_out + (c16 >> 3) * BOX_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4), w[0], w[1],
+                       w[2], w[3]);
         }
       }
+      fence_proxy_async_smem();
     }
     tc_fence_before();
     named_bar_sync(1 + g, 128);
-    if (have && half < 0 && !*abort_flag) {
-      uint8_t* gout = reinterpret_cast<uint8_t*>(g == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * N + k0) * D * 2;
-      constexpr int CHUNKS = D / 8;
-      for (int idx = row; idx < BN * CHUNKS; idx += 128) {
-        const int rr = idx / CHUNKS, c16 = idx % CHUNKS;
-        if (k0 + rr < N)
-          st_global_v4(gout + static_cast<size_t>(rr) * (2 * D) + c16 * 16,
-                       ld_shared_v4(stage_out + rr * (2 * C::DP) + ((c16 ^ (rr & 7)) << 4)));
-      }
+    if (have && half < 0 && !*abort_flag && (row & 127) == 0) {
+      const CUtensorMap* out = g == 0 ? &tmdv : &tmdk;
+      for (int b = 0; b < C::BOXES; ++b) tma_store_3d(out, stage_out + b * BOX_BYTES, 64 * b, k0, bh);
+      bulk_commit_group();
+      // the stores have read the staging before the CTA's shared memory is
+      // released; their global writes complete before the kernel does, so the
+      // SM can start its next CTA meanwhile
+      bulk_wait_read_all();
     }
   }
 
@@ -607,7 +613,8 @@ cudaError_t launch_main(const BwdParams& p, const BwdMaps& m, unsigned grid, cud
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  fa_bwd_bf16_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, m.dq_acc, p);
+  fa_bwd_bf16_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM_BYTES, s>>>(m.q, m.k, m.v, m.dO, m.dq_acc, m.dk, m.dv,
+                                                                           p);
   return cudaGetLastError();
 }
 

@@ -347,7 +347,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   BwdMaps m;
   if (!make_map_bf16(&m.q, q, p.BH, N, d, kBwdBlockRows) || !make_map_bf16(&m.k, k, p.BH, N, d, kBwdBlockCols) ||
       !make_map_bf16(&m.v, v, p.BH, N, d, kBwdBlockCols) || !make_map_bf16(&m.dO, dO, p.BH, N, d, kBwdBlockRows) ||
-      !make_map_f32_acc(&m.dq_acc, p.dq_acc, p.BH, N, d, kBwdBlockRows))
+      !make_map_f32_acc(&m.dq_acc, p.dq_acc, p.BH, N, d, kBwdBlockRows) ||
+      !make_map_bf16(&m.dk, dk, p.BH, N, d, kBwdBlockCols) || !make_map_bf16(&m.dv, dv, p.BH, N, d, kBwdBlockCols))
     return FA_ERR_CUDA;
   const cudaError_t e = launch_bwd_bf16_tc(p, m, s);
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;

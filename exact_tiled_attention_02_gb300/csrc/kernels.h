@@ -74,6 +74,7 @@ struct FwdMaps {
 struct BwdMaps {
   CUtensorMap q, k, v, dO;
   CUtensorMap dq_acc;  // fp32 [BH, N, d] accumulator: dims (d, N, BH), box (32, 128, 1), 128-byte swizzle
+  CUtensorMap dk, dv;  // the bf16 outputs, for TMA stores: as q (box (64, 128, 1), 128-byte swizzle)
 };
 
 // Launchers (each returns the launch's cudaError_t).
