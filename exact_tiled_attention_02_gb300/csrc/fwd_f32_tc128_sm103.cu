@@ -16,15 +16,19 @@
 // cannot hold Q's two parts (128 KB) beside the K and V^T tiles.  Q lives in
 // tensor memory instead, as the A operand of S = Q K^T: each softmax thread
 // reads its own query row once, splits it and stores both parts (256
-// columns).  With O (128 columns) and one S buffer (S, then P hi over it, P
-// lo beside it: 128 columns) tensor memory is full, so each 64-key tile runs
-// S_j, then the softmax, then P_j V_j in sequence; one K slot and one V^T slot
-// are enough, each refilled while the other tile's products run.
+// columns).  Beside O (128 columns) that leaves two 64-column S buffers, P hi
+// written over S; P lo goes to shared memory (two buffers) and enters P V as
+// the A operand of the P_lo V_hi products.  The tensor core then runs
+// S_0, S_1, P_0 V_0, S_2, P_1 V_1, ...: S_{j+1} runs while the softmax turns
+// S_j into P_j.  (With P lo in tensor memory beside a single S buffer, each
+// tile ran S_j, the softmax and P_j V_j in sequence, the tensor pipe busy 45%
+// of cycles.)  K and V^T each stream through a single slot: K_{j+1} loads
+// once S_j has read K_j, V_{j+1} once P_j V_j has read V_j.
 //
 // CTA: one 128-row query tile of one head, 192 threads: warps 0-3 softmax
 // (thread = row = TMEM lane), warp 4 TMEM owner + MMA issuer, warp 5 TMA
 // producer.  Tensor memory: Q hi [0,128), Q lo [128,256), O [256,384),
-// S / P hi [384,448), P lo [448,512).
+// S / P hi of tiles j = b (mod 2) at [384 + 64b, 448 + 64b).
 #include "kernels.h"
 #include "sm103.cuh"
 #include "sm103_tf32.cuh"
@@ -39,18 +43,21 @@ constexpr int BR = 128;  // query rows per CTA
 constexpr int BC = 64;   // keys per tile
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr uint32_t TM_QH = 0, TM_QL = 128, TM_O = 256, TM_S = 384, TM_PL = 448;
+constexpr uint32_t TM_QH = 0, TM_QL = 128, TM_O = 256, TM_S = 384;  // S buffer b at TM_S + 64 b
 constexpr float kRescaleThreshold = 8.0f;  // lazy rescaling, as in the other forward kernels
 // shared memory: fp32 boxes of 32 columns (128-byte rows), 128-byte swizzle
 constexpr int K_BOX = BC * 128;    // K part [64 keys][32 dims]: 8 KB
 constexpr int K_PART = 4 * K_BOX;  // K hi or lo of a tile, [64][128]: 32 KB
 constexpr int V_BOX = DP * 128;    // V^T part [128 dims][32 keys]: 16 KB
 constexpr int V_PART = 2 * V_BOX;  // V^T hi or lo of a tile, [128][64]: 32 KB
+constexpr int PL_BOX = BR * 128;   // P lo [128 rows][32 keys]: 16 KB
+constexpr int PL_BUF = 2 * PL_BOX; // P lo of a tile, [128][64]: 32 KB
 constexpr int OFF_K = 0;                    // K hi, then K lo
 constexpr int OFF_V = OFF_K + 2 * K_PART;   // V^T hi, then V^T lo
-constexpr int OFF_BAR = OFF_V + 2 * V_PART;
-// q_ready, k_full, k_empty, v_full, v_empty, s_full, p_full, drain
-constexpr int NBAR = 8;
+constexpr int OFF_PL = OFF_V + 2 * V_PART;  // P lo of tiles j = b (mod 2) at OFF_PL + b PL_BUF
+constexpr int OFF_BAR = OFF_PL + 2 * PL_BUF;
+// q_ready, k_full, k_empty, v_full, v_empty, s_full[2], p_full[2], o_done, drain
+constexpr int NBAR = 11;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
@@ -63,9 +70,10 @@ struct Bars {
   __device__ uint32_t k_empty() const { return base + 16; }
   __device__ uint32_t v_full() const { return base + 24; }
   __device__ uint32_t v_empty() const { return base + 32; }
-  __device__ uint32_t s_full() const { return base + 40; }
-  __device__ uint32_t p_full() const { return base + 48; }
-  __device__ uint32_t drain() const { return base + 56; }
+  __device__ uint32_t s_full(int b) const { return base + 40 + 8 * b; }
+  __device__ uint32_t p_full(int b) const { return base + 56 + 8 * b; }
+  __device__ uint32_t o_done() const { return base + 72; }
+  __device__ uint32_t drain() const { return base + 80; }
 };
 
 template <bool WIN>
@@ -104,8 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.k_empty(), 1);
     mbar_init(bar.v_full(), 1);
     mbar_init(bar.v_empty(), 1);
-    mbar_init(bar.s_full(), 1);
-    mbar_init(bar.p_full(), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar.s_full(b), 1);
+      mbar_init(bar.p_full(b), 4);
+    }
+    mbar_init(bar.o_done(), 1);
     mbar_init(bar.drain(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -155,10 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         vq = j + 1;
       };
-      // consumption order S_0, P_0 V_0, S_1, P_1 V_1, ...: K_{j+1} loads once
-      // S_j has read K_j, V_{j+1} once P_j V_j has read V_j
-      for (int j = 0; ok && j < ntiles; ++j) {
-        load_k(j);
+      // consumption order S_0, S_1, P_0 V_0, S_2, P_1 V_1, S_3, ...: K_j loads
+      // once S_{j-1} has read K_{j-1}, V_j once P_{j-1} V_{j-1} has read V_{j-1}
+      if (ntiles > 0) load_k(0);
+      if (ok && ntiles > 0) load_v(0);
+      if (ok && ntiles > 1) load_k(1);
+      for (int j = 1; ok && j < ntiles; ++j) {
+        if (j + 1 < ntiles) load_k(j + 1);
         if (ok) load_v(j);
       }
       if (*abort_flag) {
@@ -173,36 +187,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_tf32_f32(BR, BC);  // S: N = 64 keys
       constexpr uint32_t idesc_o = idesc_tf32_f32(BR, DP);  // P V: N = 128 dims
-      bool ok = mbar_wait(bar.q_ready(), 0, wc);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        // S_j = Q K_j^T (A = Q from tensor memory; S_j's columns were last read
-        // by P_{j-1} V_{j-1}, issued before)
-        if (!mbar_wait(bar.k_full(), j & 1, wc)) break;
+      // S_m = Q K_m^T into S buffer m % 2 (A = Q from tensor memory; the
+      // buffer's previous P hi was read by P_{m-2} V_{m-2}, issued before)
+      auto issue_s = [&](int m) -> bool {
+        if (!mbar_wait(bar.k_full(), m & 1, wc)) return false;
         tc_fence_after();
+        const uint32_t d_s = tmem + TM_S + 64 * (m & 1);
 #pragma unroll
         for (int kk = 0; kk < DP / 8; ++kk) {  // 8 dimensions (32 bytes) per step
           const uint32_t ok_ = (kk >> 2) * K_BOX + (kk & 3) * 32;
           const uint64_t kh = sdesc_sw128(sb + OFF_K + ok_, 16, 1024);
           const uint64_t kl = sdesc_sw128(sb + OFF_K + K_PART + ok_, 16, 1024);
-          mma_tf32_ts(tmem + TM_S, tmem + TM_QH + 8 * kk, kh, idesc_s, kk > 0);
-          mma_tf32_ts(tmem + TM_S, tmem + TM_QH + 8 * kk, kl, idesc_s, 1);
-          mma_tf32_ts(tmem + TM_S, tmem + TM_QL + 8 * kk, kh, idesc_s, 1);
+          mma_tf32_ts(d_s, tmem + TM_QH + 8 * kk, kh, idesc_s, kk > 0);
+          mma_tf32_ts(d_s, tmem + TM_QH + 8 * kk, kl, idesc_s, 1);
+          mma_tf32_ts(d_s, tmem + TM_QL + 8 * kk, kh, idesc_s, 1);
         }
         mma_commit(bar.k_empty());
-        mma_commit(bar.s_full());
-        // O (+)= P_j V_j
-        if (!mbar_wait2(bar.p_full(), j & 1, bar.v_full(), j & 1, wc)) break;
+        mma_commit(bar.s_full(m & 1));
+        return true;
+      };
+      bool ok = mbar_wait(bar.q_ready(), 0, wc);
+      if (ok && ntiles > 0) ok = issue_s(0);
+      if (ok && ntiles > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        // O (+)= P_j V_j: P hi from tensor memory, P lo from shared memory
+        if (!mbar_wait2(bar.p_full(j & 1), (j >> 1) & 1, bar.v_full(), j & 1, wc)) break;
         tc_fence_after();
+        const uint32_t a_hi = tmem + TM_S + 64 * (j & 1);
+        const uint32_t pl = sb + OFF_PL + (j & 1) * PL_BUF;
 #pragma unroll
         for (int kk = 0; kk < BC / 8; ++kk) {  // 8 keys per step
           const uint32_t ov = (kk >> 2) * V_BOX + (kk & 3) * 32;
           const uint64_t vh = sdesc_sw128(sb + OFF_V + ov, 16, 1024);
           const uint64_t vl = sdesc_sw128(sb + OFF_V + V_PART + ov, 16, 1024);
-          mma_tf32_ts(tmem + TM_O, tmem + TM_S + 8 * kk, vh, idesc_o, (j > 0 || kk > 0));
-          mma_tf32_ts(tmem + TM_O, tmem + TM_S + 8 * kk, vl, idesc_o, 1);
-          mma_tf32_ts(tmem + TM_O, tmem + TM_PL + 8 * kk, vh, idesc_o, 1);
+          const uint64_t al = sdesc_sw128(pl + (kk >> 2) * PL_BOX + (kk & 3) * 32, 16, 1024);
+          mma_tf32_ts(tmem + TM_O, a_hi + 8 * kk, vh, idesc_o, (j > 0 || kk > 0));
+          mma_tf32_ts(tmem + TM_O, a_hi + 8 * kk, vl, idesc_o, 1);
+          mma_tf32_ss(tmem + TM_O, al, vh, idesc_o, 1);
         }
         mma_commit(bar.v_empty());
+        mma_commit(bar.o_done());
+        if (j + 2 < ntiles && !issue_s(j + 2)) break;
       }
       mma_commit(bar.drain());
       WaitCtl drain{nullptr, nullptr, wc.limit_ns};
@@ -246,16 +271,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      // S_j has completed, and with it P_{j-1} V_{j-1} (issued before it): O
-      // may be rescaled now, before P_j V_j
-      if (!warp_wait(bar.s_full(), j & 1)) {
+      // S_j has completed, and with it P_{j-2} V_{j-2} (issued before it),
+      // the last reader of this tile's P lo buffer
+      const uint32_t tS = tl + TM_S + 64 * (j & 1);
+      if (!warp_wait(bar.s_full(j & 1), (j >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[BC];
-      tmem_ld_32x32b_x32(tl + TM_S, &sr[0]);
-      tmem_ld_32x32b_x32(tl + TM_S + 32, &sr[32]);
+      tmem_ld_32x32b_x32(tS, &sr[0]);
+      tmem_ld_32x32b_x32(tS + 32, &sr[32]);
       tmem_wait_ld();
       float sv[BC];
 #pragma unroll
@@ -288,7 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
       float rsum = 0.f;
       // P = 2^(s * scale * log2 e - m_ref) in fp32: hi over S's columns (read
-      // above), lo beside them
+      // above), lo to shared memory as this row of a [128 rows][32 keys]
+      // 128-byte-swizzled box per 32 keys (the layout the P_lo V_hi products
+      // read, K-major)
+      const uint32_t plrow = sb + OFF_PL + (j & 1) * PL_BUF + row * 128;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t ph[32], pl[32];
@@ -300,10 +329,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph[c] = __float_as_uint(hi);
           pl[c] = __float_as_uint(tf32_rna(pv - hi));
         }
-        tmem_st_32x32b_x32(tl + TM_S + 32 * h, ph);
-        tmem_st_32x32b_x32(tl + TM_PL + 32 * h, pl);
+        tmem_st_32x32b_x32(tS + 32 * h, ph);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          st_shared_v4(plrow + h * PL_BOX + ((c4 ^ (row & 7)) << 4), pl[4 * c4], pl[4 * c4 + 1], pl[4 * c4 + 2],
+                       pl[4 * c4 + 3]);
       }
+      fence_proxy_async_smem();
+      // O may be rescaled once P_{j-1} V_{j-1} has completed
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!warp_wait(bar.o_done(), (j - 1) & 1)) {
+          tmem_wait_st();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < DP / 32; ++c) {
           uint32_t o[32];
@@ -317,10 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full());
+      if (lane == 0) mbar_arrive(bar.p_full(j & 1));
       l = l * alpha + rsum;
     }
-    // every MMA has completed once the drain commit has
+    // Up to two P V products may still be running here (S_{T-1} was issued
+    // before P_{T-2} V_{T-2}), so o_done's parity cannot tell the last one
+    // apart; the drain commit, issued after every product, can
     const bool have = ok && ntiles > 0 && warp_wait(bar.drain(), 0);
     if (have && !*abort_flag) {
       // tcgen05.ld is warp-collective: every lane loads, rows past N store nothing
