@@ -362,8 +362,11 @@ def main():
         kernels["bwd"] = {"ms": bwd_ms, "tflops": flops_bwd / (bwd_ms * 1e-3) / 1e12}
         kernels["bwd"]["frac"] = kernels["bwd"]["tflops"] / peak
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    kname = {"fwd": "fwd_keymajor_sm103" if key_major else "fwd_f32_tc_sm103" if tf32x3 else
-             "fwd_f32_simt" if w.dtype == "f32" else "fwd_bf16_d256_sm103" if w.d == 256 else "fwd_bf16_sm103",
+    win_kernel = w.dtype == "bf16" and w.d != 256 and 0 < w.window <= 257  # radius <= 128
+    kname = {"fwd": "fwd_keymajor_sm103" if key_major else
+             ("fwd_f32_tc128_sm103" if w.d > 64 else "fwd_f32_tc_sm103") if tf32x3 else
+             "fwd_f32_simt" if w.dtype == "f32" else "fwd_bf16_d256_sm103" if w.d == 256 else
+             "fwd_bf16_win_sm103" if win_kernel else "fwd_bf16_sm103",
              "bwd": "bwd_f32_simt" if w.dtype == "f32" else "bwd_bf16_d64_sm103" if w.d == 64 else
              "bwd_bf16_sm103"}[dom]
     traffic = ncu_traffic(f"{kname}_{w.name}.md", kname + ".cu")
