@@ -30,15 +30,19 @@
 // 384 threads (512 for unmasked d = 128):
 //   warps 0-3  softmax for Q0: thread t owns row t of Q0 (TMEM lane t)
 //   warps 4-7  softmax for Q1: thread t owns row t of Q1 (TMEM lane t)
-//   warp  8    TMEM owner + tcgen05.mma issuer (one elected lane)
+//   warp  8    TMEM owner + tcgen05.mma issuer (one elected lane); for
+//              unmasked d = 64 only the Q K^T products
 //   warp  9    TMA producer (one elected lane)
-//   warps 10-11 idle (registers are granted per warpgroup of four warps, so
-//              a ten-warp CTA costs as much as twelve; 168 per thread)
+//   warp  10   (unmasked d = 64) issues the P V products
+//   warps 10-11 otherwise idle (registers are granted per warpgroup of four
+//              warps, so a ten-warp CTA costs as much as twelve; 168 per thread)
 //   warps 12-15 (unmasked d = 128) rescale O when a row's reference maximum
 //              moves, one warp per TMEM lane quarter (see corr_warps)
 // Tensor memory (512 columns x 128 lanes, 32-bit):
 //   [0,128) S0 (P0 as packed bf16 in its first 64 columns), [128,256) S1 / P1,
-//   [256,256+DP) O0, [384,384+DP) O1 (DP = D rounded up to 64: see Cfg).
+//   [256,256+DP) O0, [384,384+DP) O1 (DP = D rounded up to 64: see Cfg);
+//   unmasked d = 64: three S / P buffers [0,384) taken in turn, O0 at 384,
+//   O1 at 448 (see tri_s).
 // Shared memory (1024-byte aligned, 128-byte swizzled): Q0, Q1, a ring of
 // STAGES K/V tiles, barriers.
 // The two query tiles ping-pong: while the softmax warps of one tile turn
@@ -81,8 +85,25 @@ constexpr int kRegsSoftmax = 152;
 constexpr int kRegsOther = 104;
 static_assert(2 * kRegsSoftmax + 2 * kRegsOther == 4 * 128, "register shares must add up to the launch allocation");
 constexpr int kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // + 128 * tile
-constexpr uint32_t kTmemO = 256;  // + 128 * tile
+// Unmasked d = 64 keeps three S buffers instead of two: its S and O of both
+// tiles take 2 x (128 + 64) columns, and the last 128 hold a third S, so that
+// the S of a tile's next key tile is computed a whole step ahead, and it
+// issues its products from two threads (S from warp 8, P V from warp 10).
+// Measured on 4x16x2048x64: one S per tile and one issuing thread, 2665
+// cycles per key step for 1280 cycles of products; three buffers, 2650
+// (a single issuer spent ~1100 cycles a step on waits and bookkeeping between
+// instructions, each of which takes about as long to issue as to execute at
+// these sizes); three buffers and two issuers, ~2250; forward 0.0963 ->
+// 0.0761 ms.
+template <int D, bool WIN>
+constexpr bool tri_s() {
+  return D == 64 && !WIN;
+}
+constexpr uint32_t tm_s(int b) { return 128u * static_cast<uint32_t>(b); }  // S buffer b (P over its first half)
+template <int D, bool WIN>
+constexpr uint32_t tm_o(int t) {  // O of query tile t
+  return tri_s<D, WIN>() ? 384u + 64u * static_cast<uint32_t>(t) : 256u + 128u * static_cast<uint32_t>(t);
+}
 // Lazy rescaling: a row's reference maximum is raised only when a new score
 // exceeds it by more than 2^8 in linear terms.  The final O / l uses the same
 // reference for numerator and denominator, so the result is the same exact
@@ -142,9 +163,9 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // q_full[2], q_empty[2], k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain,
-  // o_staged[2], o_free, alpha_ready[2]
-  static constexpr int NBAR = 4 + 3 * STAGES + 12;
+  // q_full[2], q_empty[2], k_full[S], v_full[S], kv_empty[S], s_full[3], p_full[3], o_done[2], drain,
+  // o_staged[2], o_free, alpha_ready[2], pv_done[3]
+  static constexpr int NBAR = 4 + 3 * STAGES + 17;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // D = 64 leaves room for an output staging tile (bf16 [BR][DP]) that the
   // two query tiles share in turn; at DP = 128 the K/V ring takes that space
@@ -167,13 +188,16 @@ struct Bars {
   __device__ uint32_t k_full(int s) const { return base + 8 * (4 + s); }
   __device__ uint32_t v_full(int s) const { return base + 8 * (4 + STAGES + s); }
   __device__ uint32_t kv_empty(int s) const { return base + 8 * (4 + 2 * STAGES + s); }
-  __device__ uint32_t s_full(int t) const { return base + 8 * (4 + 3 * STAGES + t); }
-  __device__ uint32_t p_full(int t) const { return base + 8 * (6 + 3 * STAGES + t); }
-  __device__ uint32_t o_done(int t) const { return base + 8 * (8 + 3 * STAGES + t); }
-  __device__ uint32_t drain() const { return base + 8 * (10 + 3 * STAGES); }
-  __device__ uint32_t o_staged(int t) const { return base + 8 * (11 + 3 * STAGES + t); }
-  __device__ uint32_t o_free() const { return base + 8 * (13 + 3 * STAGES); }
-  __device__ uint32_t alpha_ready(int t) const { return base + 8 * (14 + 3 * STAGES + t); }
+  // s_full / p_full: one per S buffer (the query tile's index where a tile owns its buffer)
+  __device__ uint32_t s_full(int b) const { return base + 8 * (4 + 3 * STAGES + b); }
+  __device__ uint32_t p_full(int b) const { return base + 8 * (7 + 3 * STAGES + b); }
+  __device__ uint32_t o_done(int t) const { return base + 8 * (10 + 3 * STAGES + t); }
+  __device__ uint32_t drain() const { return base + 8 * (12 + 3 * STAGES); }
+  __device__ uint32_t o_staged(int t) const { return base + 8 * (13 + 3 * STAGES + t); }
+  __device__ uint32_t o_free() const { return base + 8 * (15 + 3 * STAGES); }
+  __device__ uint32_t alpha_ready(int t) const { return base + 8 * (16 + 3 * STAGES + t); }
+  // three-buffer layout: the P V that read S buffer b has completed
+  __device__ uint32_t pv_done(int b) const { return base + 8 * (18 + 3 * STAGES + b); }
 };
 
 // The key tiles of one item: [j_lo, j_lo + ntiles), and each query tile's own
@@ -261,17 +285,21 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar.q_full(t), 1);
       mbar_init(bar.q_empty(t), 1);
-      mbar_init(bar.s_full(t), 1);
-      mbar_init(bar.p_full(t), corr_warps<D, WIN>() ? 8 : 4);  // the tile's softmax warps (+ correction warps)
       mbar_init(bar.alpha_ready(t), 4);
       mbar_init(bar.o_done(t), 1);
+    }
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(bar.s_full(b), 1);
+      mbar_init(bar.p_full(b), corr_warps<D, WIN>() ? 8 : 4);  // the softmax warps of a tile (+ correction warps)
+      mbar_init(bar.pv_done(b), 1);
     }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar.k_full(s), 1);
       mbar_init(bar.v_full(s), 1);
-      mbar_init(bar.kv_empty(s), 1);
+      // three-buffer layout: released by both MMA issuers (the S and the P V products)
+      mbar_init(bar.kv_empty(s), tri_s<D, WIN>() ? 2 : 1);
     }
-    mbar_init(bar.drain(), 1);
+    mbar_init(bar.drain(), tri_s<D, WIN>() ? 2 : 1);
     mbar_init(bar.o_staged(0), 128);  // staged output: every thread of the tile, after its row
     mbar_init(bar.o_staged(1), 128);
     mbar_init(bar.o_free(), 4);       // ... one arrive per warp of the tile that just stored
@@ -324,7 +352,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
                 break;
               }
               tc_fence_after();
-              const uint32_t tO = tlq + kTmemO + t * 128;
+              const uint32_t tO = tlq + tm_o<D, WIN>(t);
               const float2 a2 = make_float2(a, a);
 #pragma unroll
               for (int c = 0; c < D / 32; ++c) {
@@ -379,14 +407,17 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
             break;
           }
           const int kv0 = (w.j_lo + it) * BC;
-          mbar_arrive_expect_tx(bar.k_full(st), C::KV_BYTES);
+          // three-buffer layout: K and V of a slot complete one barrier, so a
+          // P (computed from an S that read K) implies its V is resident too
+          const uint32_t vbar = tri_s<D, WIN>() ? bar.k_full(st) : bar.v_full(st);
+          mbar_arrive_expect_tx(bar.k_full(st), tri_s<D, WIN>() ? 2 * C::KV_BYTES : C::KV_BYTES);
 #pragma unroll
           for (int b = 0; b < C::BOXES; ++b)
             tma_load_3d(sK + st * C::KV_BYTES + b * BC * 128, &tmk, bar.k_full(st), b * 64, kv0, w.bh);
-          mbar_arrive_expect_tx(bar.v_full(st), C::KV_BYTES);
+          if (!tri_s<D, WIN>()) mbar_arrive_expect_tx(bar.v_full(st), C::KV_BYTES);
 #pragma unroll
           for (int b = 0; b < C::BOXES; ++b)
-            tma_load_3d(sV + st * C::KV_BYTES + b * BC * 128, &tmv, bar.v_full(st), b * 64, kv0, w.bh);
+            tma_load_3d(sV + st * C::KV_BYTES + b * BC * 128, &tmv, vbar, b * 64, kv0, w.bh);
         }
       }
       if (*abort_flag) {
@@ -398,7 +429,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         }
         for (int s = max(0, g - C::STAGES); s < g; ++s) {
           mbar_wait(bar.k_full(s % C::STAGES), (s / C::STAGES) & 1, drain);
-          mbar_wait(bar.v_full(s % C::STAGES), (s / C::STAGES) & 1, drain);
+          if (!tri_s<D, WIN>()) mbar_wait(bar.v_full(s % C::STAGES), (s / C::STAGES) & 1, drain);
         }
       }
     }
@@ -413,7 +444,11 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       int cnt[2] = {0, 0};      // key tiles each query tile has processed (all items)
       int nq = 0;               // items started
       int last[2] = {0, 0};     // index of each tile's last key tile in the current item
-      auto issue_s = [&](int t, int it) {  // S_t = Q_t K_it^T
+      // three-buffer layout: S products issued (all items), the buffer of the
+      // next one and that buffer's phase parity; the K/V ring slot and parity
+      int ks = 0, bs = 0, rs = 0;
+      uint32_t bq = 0, rp = 0;
+      auto issue_s = [&](int t, int it, int b) {  // S_t = Q_t K_it^T into S buffer b
         // descriptors built once per tile, advanced by their address field
         // (16-byte units) per K-step: the MMA warp shares its SM
         // sub-partition with two softmax warps, and rebuilding both 64-bit
@@ -423,7 +458,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         // never carries into the neighbouring offset fields.
         const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
         const uint64_t dk = sdesc_sw128(sK + ((g0 + it) % C::STAGES) * C::KV_BYTES, 16, 1024);
-        const uint32_t dt = tmem + kTmemS + t * 128;
+        const uint32_t dt = tmem + tm_s(b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offq = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
@@ -433,12 +468,12 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
           else
             mma_bf16_ss(dt, dq + (offq >> 4), dk + (offk >> 4), idesc_qk, kk > 0);
         }
-        mma_commit(bar.s_full(t));
+        mma_commit(bar.s_full(b));
         if (it == last[t]) mma_commit(bar.q_empty(t));  // Q_t is free once this product completes
       };
-      auto issue_pv = [&](int t, int it, bool first) {  // O_t (+)= P_t V_it
+      auto issue_pv = [&](int t, int it, bool first, int b) {  // O_t (+)= P_t V_it, P_t in S buffer b
         const uint64_t dv = sdesc_sw128(sV + ((g0 + it) % C::STAGES) * C::KV_BYTES, BC * 128, 1024);
-        const uint32_t dt = tmem + kTmemO + t * 128, at = tmem + kTmemS + t * 128;
+        const uint32_t dt = tmem + tm_o<D, WIN>(t), at = tmem + tm_s(b);
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
           if constexpr (D != 64)
@@ -461,13 +496,51 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
           last[t] = w.hi[t] - 1;
           if (w.lo[t] >= w.hi[t]) mma_commit(bar.q_empty(t));  // no product reads Q_t in this item
         }
-        if (!WIN && w.lo[1] < w.hi[1]) {
+        if constexpr (tri_s<D, WIN>()) {
+          // Three S buffers, taken in turn by the S products in issue order
+          // (index ks counts them across items): S0(0) S1(0) S0(1) S1(1) ...
+          // for a pair of tiles, S(0) S(1) ... for a single tile.  This
+          // thread issues only the S products; warp 10 issues the P V
+          // products (role_pv), so that neither thread's waits and
+          // bookkeeping hold up the tensor core (one thread issuing every
+          // product left it idle about half the time: issuing an
+          // instruction takes nearly as long as executing one at these
+          // sizes).  S(k) overwrites buffer k % 3 once the P V that read
+          // S(k - 3) there has completed (pv_done), so every tile's next S
+          // is computed while its softmax works on the current one.
+          const bool pair = w.lo[1] < w.hi[1];
+          for (int it = 0; ok && it < w.ntiles; ++it) {
+            if (!mbar_wait(bar.k_full(rs), rp, wc)) {  // K_it and V_it resident
+              ok = false;
+              break;
+            }
+            for (int t = 0; t < (pair ? 2 : 1); ++t) {
+              if (ks >= 3 && !mbar_wait(bar.pv_done(bs), bq ^ 1u, wc)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(t, it, bs);
+              ++ks;
+              if (++bs == 3) {
+                bs = 0;
+                bq ^= 1u;
+              }
+            }
+            if (!ok) break;
+            mma_commit(bar.kv_empty(rs));  // this issuer's share of the slot's release
+            if (++rs == C::STAGES) {
+              rs = 0;
+              rp ^= 1u;
+            }
+          }
+        } else if (!WIN && w.lo[1] < w.hi[1]) {
           // both tiles take every key tile: PV0(j), S0(j+1), PV1(j), release, S1(j+1)
           ok = wait_k(0);
           if (ok) {
             tc_fence_after();
-            issue_s(0, 0);
-            issue_s(1, 0);
+            issue_s(0, 0, 0);
+            issue_s(1, 0, 1);
           }
           for (int it = 0; ok && it < w.ntiles; ++it) {
             const int g = g0 + it;
@@ -486,7 +559,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
               break;
             }
             tc_fence_after();
-            issue_pv(0, it, it == 0);
+            issue_pv(0, it, it == 0, 0);
             if (more) {
               if (!k_early) {
                 if (!wait_k(it + 1)) {
@@ -495,16 +568,16 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
                 }
                 tc_fence_after();
               }
-              issue_s(0, it + 1);
+              issue_s(0, it + 1, 0);
             }
             if (!mbar_wait(bar.p_full(1), (cnt[1] + it) & 1, wc)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_pv(1, it, it == 0);
+            issue_pv(1, it, it == 0, 1);
             mma_commit(bar.kv_empty(st));  // before S1(j+1): a commit waits for every earlier MMA
-            if (more) issue_s(1, it + 1);
+            if (more) issue_s(1, it + 1, 1);
           }
           cnt[0] += w.ntiles;
           cnt[1] += w.ntiles;
@@ -515,7 +588,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
             ok = wait_k(w.lo[t]);
             if (ok) {
               tc_fence_after();
-              issue_s(t, w.lo[t]);
+              issue_s(t, w.lo[t], t);
             }
           }
           int c[2] = {0, 0};
@@ -535,7 +608,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
                 break;
               }
               tc_fence_after();
-              issue_pv(t, it, c[t] == 0);
+              issue_pv(t, it, c[t] == 0, t);
               ++c[t];
               if (t == 1 || it < w.lo[1] || it >= w.hi[1]) mma_commit(bar.kv_empty(st));
               if (it + 1 < w.hi[t]) {
@@ -544,7 +617,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
                   break;
                 }
                 tc_fence_after();
-                issue_s(t, it + 1);
+                issue_s(t, it + 1, t);
               }
             }
           }
@@ -560,12 +633,60 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
     }
     __syncwarp();
   };
+  auto role_pv = [&]() {
+    // ---------------------------------------------- P V issuer (warp 10)
+    // (three-buffer layout) O_t += P_t V_j for every P in the order the S
+    // products were issued: the k-th P lives in S buffer k % 3 and completes
+    // phase k / 3 of that buffer's p_full barrier.  A P implies its V is
+    // resident: K and V of a slot complete one barrier, which the S product
+    // that P was computed from waited for.
+    if constexpr (tri_s<D, WIN>()) {
+      if (lane == 0) {
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(BR, C::DP, 0, 1);
+        int bs = 0, rs = 0;
+        uint32_t bq = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+          const Item w = decode_item<WIN>(item, N, r, n_pair);
+          const bool pair = w.lo[1] < w.hi[1];
+          for (int it = 0; ok && it < w.ntiles; ++it) {
+            const uint64_t dv = sdesc_sw128(sV + rs * C::KV_BYTES, BC * 128, 1024);
+            for (int t = 0; t < (pair ? 2 : 1); ++t) {
+              if (!mbar_wait(bar.p_full(bs), bq, wc)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t dt = tmem + tm_o<D, WIN>(t), at = tmem + tm_s(bs);
+#pragma unroll
+              for (int kk = 0; kk < BC / 16; ++kk)
+                mma_bf16_ts(dt, at + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (it > 0 || kk > 0));
+              mma_commit(bar.o_done(t));
+              mma_commit(bar.pv_done(bs));
+              if (++bs == 3) {
+                bs = 0;
+                bq ^= 1u;
+              }
+            }
+            if (!ok) break;
+            mma_commit(bar.kv_empty(rs));  // this issuer's share of the slot's release
+            if (++rs == C::STAGES) rs = 0;
+          }
+        }
+        // every product this thread issued must finish before tensor memory is freed
+        mma_commit(bar.drain());
+        WaitCtl drain{nullptr, nullptr, wc.limit_ns};
+        mbar_wait(bar.drain(), 0, drain);
+      }
+      __syncwarp();
+    }
+  };
   auto role_softmax = [&]() {
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t tS = tl + kTmemS + t * 128, tO = tl + kTmemO + t * 128;
+    const uint32_t tO = tl + tm_o<D, WIN>(t);
     const float sl = p.scale_log2;
     bool ok = true;
     // windowed items are short, and there the staged path measured 7% slower
@@ -573,6 +694,7 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
     int n = 0;   // key tiles this warpgroup has processed (all items)
     int ni = 0;  // items this warpgroup has passed (both warpgroups see every item)
     int no = 0;  // outputs this warpgroup has staged
+    int ks = 0;  // S products of all items before this one (three-buffer layout; as counted by the MMA role)
     auto warp_wait = [&](uint32_t bar_addr, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
     };
@@ -583,8 +705,18 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
       // l: row sum of the unrounded P (lse uses it); lc: the bf16 rounding
       // error of each tile's largest P, which O's normaliser adds (below)
       float m_ref = -INFINITY, l = 0.f, lc = 0.f;
+      const bool pair = w.lo[1] < w.hi[1];
       for (int it = w.lo[t]; it < w.hi[t]; ++it, ++n) {
-        if (!warp_wait(bar.s_full(t), n & 1)) {
+        // this tile's S buffer and the phase it completes there
+        int sb = t;
+        uint32_t sph = n & 1;
+        if constexpr (tri_s<D, WIN>()) {
+          const int k = pair ? ks + 2 * it + t : ks + it;
+          sb = k % 3;
+          sph = (k / 3) & 1;
+        }
+        const uint32_t tS = tl + tm_s(sb);
+        if (!warp_wait(bar.s_full(sb), sph)) {
           ok = false;
           break;
         }
@@ -680,10 +812,11 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar.p_full(t));
+        if (lane == 0) mbar_arrive(bar.p_full(sb));
         l = l * alpha + rsum;
       }
       if (!ok) break;
+      ks += pair ? 2 * w.ntiles : w.ntiles;
       // ------------------------------------------------------------ output
       // With a staging tile (D = 64), O goes out through shared memory: each
       // thread writes its normalised row (16-byte chunks XOR-swizzled by row),
@@ -795,7 +928,8 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
     }
   } else {
     if (warp >= 10) {
-      // idle warps of the third warpgroup
+      // warp 10 issues the P V products in the three-buffer layout; otherwise idle
+      if (warp == 10) role_pv();
     } else if (warp == 9) {
       role_tma();
     } else if (warp == 8) {

@@ -115,6 +115,12 @@ BF16_CASES = [
     (1, 40, 1100, 128, 0, 8.0),
     (1, 40, 1100, 96, 0, 1.0),
     (1, 40, 1100, 64, 0, 1.0),
+    # unmasked d = 64 rotates three S buffers across items: items of one key
+    # tile (two per CTA), of three key tiles with single-tile items after
+    # them (320 pairs: the last 16 re-cut), and large logits over many items
+    (2, 100, 100, 64, 0, 1.0),
+    (1, 160, 300, 64, 0, 1.0),
+    (1, 80, 1100, 64, 0, 8.0),
     # bands wider than radius 128 run the two-tile persistent kernel; narrower
     # ones one query tile per CTA
     (1, 80, 1100, 128, 1025, 1.0),
