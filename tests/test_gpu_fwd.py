@@ -249,6 +249,30 @@ def test_full_size_workloads_every_head(index):
     assert lmax <= 1e-3, (index, lmax)
 
 
+def test_bf16_d64_long_items_every_head_sampled():
+    """Unmasked d = 64 at B=2, H=16, N=8192: 512 items of 64 key tiles each,
+    3-4 items per CTA, so the three S buffers and the per-buffer barriers of
+    both MMA issuers turn over many times within an item and across items.
+    The device status must stay clear (no wait ran out) and sampled rows of
+    every head match the oracle; every output lies in the convex hull of V."""
+    dev = _dev()
+    B, H, N, d = 2, 16, 8192, 64
+    q, k, v = inputs.make_inputs(B, H, N, d, "bf16", seed=8192 + d)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = _fa().fa_fwd(qd, kd, vd)
+    torch.cuda.synchronize()
+    assert _fa().fa_last_device_status() == 0
+    vmax = vd.float().amax(dim=2, keepdim=True)
+    vmin = vd.float().amin(dim=2, keepdim=True)
+    assert bool(((o.float() <= vmax + 2e-2) & (o.float() >= vmin - 2e-2)).all())
+    rng = np.random.default_rng(8192)
+    for b in range(B):
+        for h in range(H):
+            rows = np.sort(np.concatenate([[0, 127, 128, 255, 256, N - 1], rng.choice(N, 10, replace=False)]))
+            o_ref, lse_ref = oracle.dense_forward_rows(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), 0.125, rows)
+            _check_bf16(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, (b, h))
+
+
 @pytest.mark.parametrize("d,window", [(96, 0), (96, 257), (256, 0), (256, 257)])
 def test_bf16_other_d_large_sampled(d, window):
     """d = 96 (tiles padded to 128 columns in shared memory) and d = 256 (one
