@@ -22,15 +22,18 @@
 //   split_vt     V -> V^T hi / lo, [B*H][DP][Npad] (Npad = N rounded up to 64),
 //                so that P V reads V K-major (keys contiguous), the layout
 //                tcgen05.mma takes for tf32 operands here
-//   main         one CTA = one 128-row query tile of one head, 192 threads:
+//   main         one CTA = one 128-row query tile of one head, 224 threads:
 //                warps 0-3 softmax (thread = row = TMEM lane), warp 4 TMEM
-//                owner + MMA issuer, warp 5 TMA producer.  64-key tiles;
-//                K and V^T each stream through their own two-slot ring; S is
-//                double-buffered in tensor memory so that S_{j+1} is computed
-//                while the softmax turns S_j into P_j.  MMA order: S_0, S_1,
-//                then per key tile j: O += P_j V_j, S_{j+2} (into the buffer
-//                P_j occupied; tcgen05.mma operations of one thread execute in
-//                order).  Each product is three kind::tf32 MMAs per K-step.
+//                owner + issuer of the S products, warp 5 TMA producer, warp
+//                6 issuer of the P V products.  64-key tiles; K and V^T each
+//                stream through their own two-slot ring; S is double-buffered
+//                in tensor memory so that S_{j+1} is computed while the
+//                softmax turns S_j into P_j.  S_{j+2} goes into the buffer
+//                P_j occupied once P_j V_j has completed (pv_done).  Each
+//                product is three kind::tf32 MMAs per K-step, 24 instructions
+//                of N = 64 per product; one thread issuing both products
+//                (an instruction takes about as long to issue as to execute
+//                at N = 64) measured ~3900 cycles per key tile.
 // Tensor memory (512 columns): buffer b at 128 b: S_b / P_b hi in columns
 // [0, 64), P_b lo in [64, 128); O in [256, 320).
 #include "kernels.h"
@@ -45,7 +48,7 @@ using namespace sm103;
 constexpr int D = 64;   // padded head dimension of the split operands
 constexpr int BR = 128;  // query rows per CTA
 constexpr int BC = 64;   // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // lazy rescaling, as in the bf16 kernels
@@ -59,8 +62,8 @@ constexpr int OFF_QL = OFF_QH + Q_BYTES;
 constexpr int OFF_K = OFF_QL + Q_BYTES;       // two K slots
 constexpr int OFF_V = OFF_K + 2 * SLOT_BYTES;  // two V^T slots
 constexpr int OFF_BAR = OFF_V + 2 * SLOT_BYTES;
-// q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, drain
-constexpr int NBAR = 1 + 8 + 2 + 2 + 2;
+// q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, drain, pv_done[2]
+constexpr int NBAR = 1 + 8 + 2 + 2 + 2 + 2;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
@@ -80,6 +83,8 @@ struct Bars {
   __device__ uint32_t p_full(int b) const { return base + 8 * (11 + b); }
   __device__ uint32_t o_done() const { return base + 8 * 13; }
   __device__ uint32_t drain() const { return base + 8 * 14; }
+  // P_j V_j (buffer b = j % 2) has completed: S_{j+2} may overwrite the buffer
+  __device__ uint32_t pv_done(int b) const { return base + 8 * (15 + b); }
 };
 
 __global__ void __launch_bounds__(256) fa_split_rows_kernel(const float* __restrict__ x, float* __restrict__ hi,
@@ -151,9 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar.v_empty(s), 1);
       mbar_init(bar.s_full(s), 1);
       mbar_init(bar.p_full(s), 4);
+      mbar_init(bar.pv_done(s), 1);
     }
     mbar_init(bar.o_done(), 1);
-    mbar_init(bar.drain(), 1);
+    mbar_init(bar.drain(), 2);  // both MMA issuers
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -228,12 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 4) {
-    // ------------------------------------------------------------------ MMA
+    // ------------------------------------------------------- S products (MMA)
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32_f32(BR, 64);  // N = 64 keys for S, N = 64 dims for P V
-      auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j % 2
+      constexpr uint32_t idesc = idesc_tf32_f32(BR, 64);  // N = 64 keys
+      bool ok = mbar_wait(bar.q_full(), 0, wc);
+      for (int j = 0; ok && j < ntiles; ++j) {  // S_j = Q K_j^T into buffer j % 2
         const int s = j & 1;
-        if (!mbar_wait(bar.k_full(s), (j >> 1) & 1, wc)) return false;
+        // K_j resident; for j >= 2, P_{j-2} V_{j-2} has read the buffer
+        if (!mbar_wait(bar.k_full(s), (j >> 1) & 1, wc) ||
+            (j >= 2 && !mbar_wait(bar.pv_done(s), ((j >> 1) & 1) ^ 1, wc))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t dtm = tmem + 128 * s;
         const uint32_t kb = sb + OFF_K + s * SLOT_BYTES;
@@ -248,11 +260,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar.k_empty(s));
         mma_commit(bar.s_full(s));
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {  // O (+)= P_j V_j
+      }
+      mma_commit(bar.drain());
+      WaitCtl drain{nullptr, nullptr, wc.limit_ns};
+      mbar_wait(bar.drain(), 0, drain);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ----------------------------------------------------- P V products (MMA)
+    // every P in order, so this thread sees each phase of p_full and
+    // completes each phase of pv_done in turn
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32_f32(BR, 64);  // N = 64 dims
+      bool ok = true;
+      for (int j = 0; ok && j < ntiles; ++j) {  // O (+)= P_j V_j
         const int s = j & 1;
-        if (!mbar_wait(bar.p_full(s), (j >> 1) & 1, wc) || !mbar_wait(bar.v_full(s), (j >> 1) & 1, wc)) return false;
+        if (!mbar_wait(bar.p_full(s), (j >> 1) & 1, wc) || !mbar_wait(bar.v_full(s), (j >> 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t ph = tmem + 128 * s, pl = ph + 64;
         const uint32_t vb = sb + OFF_V + s * SLOT_BYTES;
@@ -266,14 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar.v_empty(s));
         mma_commit(bar.o_done());
-        return true;
-      };
-      bool ok = mbar_wait(bar.q_full(), 0, wc);
-      if (ok && ntiles > 0) ok = issue_s(0);
-      if (ok && ntiles > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        ok = issue_pv(j);
-        if (ok && j + 2 < ntiles) ok = issue_s(j + 2);
+        mma_commit(bar.pv_done(s));
       }
       mma_commit(bar.drain());
       WaitCtl drain{nullptr, nullptr, wc.limit_ns};
@@ -352,8 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_32x32b_x32(tS + 64 + 32 * h, pl);
       }
       // O may be rescaled only once the previous P V has completed; here
-      // P_{j-2} V_{j-2} has completed (S_j was issued after it) and P_j V_j has
-      // not been issued, so o_done is within one phase of the one waited for
+      // P_{j-2} V_{j-2} has completed (S_j was issued after its pv_done) and
+      // P_j V_j has not been issued, so o_done is within one phase of the one
+      // waited for
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         if (!warp_wait(bar.o_done(), (j - 1) & 1)) {
           tmem_wait_st();
@@ -377,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar.p_full(s));
       l = l * alpha + rsum;
     }
-    // every MMA has completed once the drain commit has (up to two P V may be
-    // in flight after the last softmax step)
+    // every MMA has completed once both issuers' drain commits have (up to two
+    // P V may be in flight after the last softmax step)
     const bool have = ok && ntiles > 0 && warp_wait(bar.drain(), 0);
     if (have && !*abort_flag) {
       // tcgen05.ld is warp-collective: every lane loads, rows past N store nothing
