@@ -33,12 +33,14 @@
 //   [0,128) S^T / P^T   [128,256) dP^T / dS^T   [256,320) dV   [320,384) dK
 //   [384,448) dQ
 // so, per step i, the MMA threads issue
-//   dV_i (once P_i is in TMEM), S^T_{i+1}, and, on the other thread,
-//   dQ_i (once dS_i is in shared memory), dK_i (once it is in TMEM), dP^T_{i+1}
+//   dV_i (once P_i is in TMEM) and S^T_{i+1}; on a second thread dK_i (once
+//   dS_i is in TMEM) and dP^T_{i+1}; on a third dQ_i (once dS_i is in shared
+//   memory)
 // and the compute warpgroups run dS_i, then P_{i+1} (its S^T_{i+1} already
 // computed), then the read-out of dQ_i: the exponentials of the next tile
-// overlap this tile's dQ and dK products.  dQ_i goes before dK_i so that it
-// is complete when the warpgroups come to read it.  Shared memory also has
+// overlap this tile's dQ and dK products.  dQ_i and dK_i go out from two
+// threads once dS_i is in place, so dQ_i need not queue behind dK_i before
+// the warpgroups come to read it.  Shared memory also has
 // room at d = 64 for a dedicated dQ staging tile and a three-stage Q/dO
 // ring, so the ring is refilled as soon as dK_i has read Q_i, independently
 // of the dQ reductions.
@@ -47,9 +49,10 @@
 // warpgroups (query columns 0-63 / 64-127 of every tile; thread t owns key
 // row t == TMEM lane t, and for the dQ read-out query row t, warpgroup g
 // taking d columns [32g, 32g + 32)); warp 8 owns TMEM and issues dV and S^T;
-// warp 10 issues dQ, dK and dP^T (measured: 2.6% faster at 2x16x8192x64
-// than one issuing thread, whose sub-partition it shares with two compute
-// warps); warp 9 is the TMA producer (loads, dQ reductions); warp 11 idles.
+// warp 10 issues dK and dP^T, warp 11 dQ (measured at 2x16x8192x64: a
+// second issuing thread, for dQ, dK and dP^T, 2.6% faster than one; dQ on a
+// third, 1.355 -> 1.324 ms); warp 9 is the TMA producer (loads, dQ
+// reductions).
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -89,8 +92,8 @@ constexpr int OFF_DST = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr int OFF_OST = OFF_DST + DST_BYTES;
 constexpr int OFF_BAR = OFF_OST + 2 * OST_BOX;
 // kv_full, st_full[3], stage_free[3], s_full, dp_full, p_full, ds_full, dq_full, staged, ost_free, fin, drain,
-// drain2
-constexpr int NBAR = 1 + 2 * STAGES + 10;
+// drain2, drain3
+constexpr int NBAR = 1 + 2 * STAGES + 11;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 // the whole 227 KB: every address an MMA operand descriptor can form (16
@@ -117,6 +120,7 @@ struct Bars {
   __device__ uint32_t fin() const { return at(7); }
   __device__ uint32_t drain() const { return at(8); }
   __device__ uint32_t drain2() const { return at(9); }
+  __device__ uint32_t drain3() const { return at(10); }
 };
 
 __host__ __device__ __forceinline__ int npad128(int n) { return (n + 127) & ~127; }
@@ -193,9 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.dq_full(), 1);
     mbar_init(bar.staged(), 8);
     mbar_init(bar.ost_free(), 1);  // the producer, once a reduction has read the staging tile
-    mbar_init(bar.fin(), 2);  // one commit per MMA-issuing thread
+    mbar_init(bar.fin(), 3);  // one commit per MMA-issuing thread
     mbar_init(bar.drain(), 1);
     mbar_init(bar.drain2(), 1);
+    mbar_init(bar.drain3(), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -219,9 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc));
   };
 
-  if (warp == 11) {
-    // idle
-  } else if (warp == 9) {
+  if (warp == 9) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmq);
@@ -273,24 +276,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 8 || warp == 10) {
+  } else if (warp == 8 || warp == 10 || warp == 11) {
     // ----------------------------------------------------------------- MMA
-    // Two issuing threads on two SM sub-partitions (each shares its
+    // Three issuing threads on three SM sub-partitions (each shares its
     // sub-partition with two compute warps, whose instructions delay the
-    // issue): warp 8 issues dV_i and S^T_{i+1}, warp 10 dQ_i, dK_i and
-    // dP^T_{i+1}.  Neither writes what the other's products read, and each
-    // thread's products run in its issue order; the stage is free once both
-    // have committed (stage_free counts two).
+    // issue; and issuing a tcgen05.mma takes about as long as executing one
+    // of N = 64): warp 8 issues dV_i and S^T_{i+1}, warp 10 dK_i and
+    // dP^T_{i+1}, warp 11 dQ_i.  None writes what another's products read,
+    // and each thread's products run in its issue order; the stage is free
+    // once warps 8 and 10 have committed (stage_free counts two: dQ does not
+    // read the stage), and the epilogue once all three have (fin).
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       constexpr uint32_t id_kb = idesc_bf16_f32(128, D, 0, 1);    // A from TMEM, B MN-major, N = 64
       constexpr uint32_t id_mm = idesc_bf16_f32(128, D, 1, 1);    // both MN-major (dS, K), N = 64
       // P^T / dS^T of query columns 16kk.. sit at TMEM column 8kk, or 64 + 8(kk - 4)
       auto pcol = [](int kk) { return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); };
-      const bool first = warp == 8;
       bool ok = mbar_wait2(bar.kv_full(), 0, bar.st_full(0), 0, wc);
       if (ok) tc_fence_after();
-      if (first) {
+      if (warp == 11) {
+        // dQ_i = dS K into its own columns, once dS_i is in shared memory (the
+        // warpgroups read dQ_{i-1} out before computing dS_i: ds_full also
+        // frees the columns)
+        for (int i = 0; ok && i < nsteps; ++i) {
+          if (!mbar_wait(bar.ds_full(), i & 1, wc)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ss(tmem + TM_DQ, sdesc_sw128(sDS + kk * 2048, DST_BOX, 1024),
+                        sdesc_sw128(sK + kk * 2048, TILE_BYTES, 1024), id_mm, kk > 0);
+          mma_commit(bar.dq_full());
+        }
+        mma_commit(bar.fin());
+        mma_commit(bar.drain3());
+        WaitCtl drain{nullptr, nullptr, wc.limit_ns};
+        mbar_wait(bar.drain3(), 0, drain);
+      } else if (warp == 8) {
         // S^T_i = K Q_i^T (stage i % STAGES resident)
         auto issue_s = [&](int i) {
           const int st = i % STAGES;
@@ -347,20 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = i & 1;
           const uint32_t qb = sStage + st * STAGE_BYTES;
           const bool more = i + 1 < nsteps;
-          // dQ_i = dS K into its own columns, first, so that it is ready when the
-          // warpgroups finish the next P.  (They read dQ_{i-1} out before
-          // computing dS_i: ds_full also frees the columns.)
+          // (dQ_i is warp 11's.)  dK += dS^T Q_i (Q_i's last reader), then the
+          // next dP^T into the columns dS^T_i leaves
           if (more ? !mbar_wait2(bar.ds_full(), ph, bar.st_full((i + 1) % STAGES), ((i + 1) / STAGES) & 1, wc)
                    : !mbar_wait(bar.ds_full(), ph, wc))
             break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ss(tmem + TM_DQ, sdesc_sw128(sDS + kk * 2048, DST_BOX, 1024),
-                        sdesc_sw128(sK + kk * 2048, TILE_BYTES, 1024), id_mm, kk > 0);
-          mma_commit(bar.dq_full());
-          // dK += dS^T Q_i (Q_i's last reader), then the next dP^T into the
-          // columns dS^T_i leaves
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
             mma_bf16_ts(tmem + TM_DK, tmem + TM_DP + pcol(kk), sdesc_sw128(qb + kk * 2048, TILE_BYTES, 1024), id_kb,
