@@ -42,16 +42,32 @@ __device__ __forceinline__ uint4 bf16_split3_row(float x) {
   return v;
 }
 
-// One warp per (padded) row; each pass, lane l reads 4 consecutive bf16
-// (8 bytes) of O and dO at column 4l.  (Four rows per warp with all loads
-// issued first measured 30% slower.)
+// Lane groups of G = 8 (d = 64) or 16 (d = 96, 128) lanes per row, lane c of
+// a group holding the 16-byte chunk c (8 bf16) of O and of dO; a warp covers
+// 32 / G rows per pass and U = 4 passes, with every load of the four passes
+// issued before any is used, so that each SM has enough bytes in flight to
+// keep HBM busy.  A warp's rows are consecutive padded rows of one (batch,
+// head): np is a multiple of 128 and a warp's row count divides 128.
+template <int D>
+struct PrepShape {
+  static constexpr int CH = D / 8;                          // 16-byte chunks per row
+  static constexpr int G = CH <= 8 ? 8 : (CH <= 16 ? 16 : 32);  // lanes per row
+  static constexpr int RPW = 32 / G;                        // rows per warp and pass
+  static constexpr int U = 4;                               // passes per warp
+  static constexpr int RW = RPW * U;                        // rows per warp
+  static constexpr int RB = 8 * RW;                         // rows per 256-thread block
+  static_assert(128 % RW == 0, "a warp's rows stay within one (batch, head)");
+};
+
+template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ lse2,
                                                          float* __restrict__ dsum, float* __restrict__ dq_acc, int BH,
-                                                         int N, int d, float inv_scale, int split,
-                                                         long long row_blocks, float* __restrict__ kv_part,
-                                                         long long part4) {
+                                                         int N, float inv_scale, long long row_blocks,
+                                                         float* __restrict__ kv_part, long long part4) {
+  using S = PrepShape<D>;
+  constexpr bool kSplit = D == 64;  // the d = 64 kernel's three-term operand rows
   if (blockIdx.x >= row_blocks) {
     // zero the split tiles' partial rows, one float4 per thread
     const long long i = (static_cast<long long>(blockIdx.x) - row_blocks) * 256 + threadIdx.x;
@@ -60,51 +76,62 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int np = npad128(N);
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // padded row index
-  if (row >= static_cast<long long>(BH) * np) return;
-  const long long bh = row / np;
-  const int i = static_cast<int>(row % np);
-  if (i >= N) {
-    if (lane == 0) {
-      if (split) {
-        // -lse / scale far below any logit: the row's P underflows to 0
-        reinterpret_cast<uint4*>(lse2)[row] = bf16_split3_row(-1e30f);
-        reinterpret_cast<uint4*>(dsum)[row] = bf16_split3_row(0.f);
-      } else {
-        lse2[row] = -INFINITY;
-        dsum[row] = 0.f;
-      }
-    }
-    return;
-  }
-  const long long src = (bh * N + i) * d;
-  float acc = 0.f;
-  for (int c = lane * 4; c < d; c += 128) {
-    const uint2 ov = *reinterpret_cast<const uint2*>(o + src + c);
-    const uint2 gv = *reinterpret_cast<const uint2*>(dO + src + c);
-    const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
-    const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+  const long long base = (static_cast<long long>(blockIdx.x) * 8 + warp) * S::RW;  // first padded row of the warp
+  if (base >= static_cast<long long>(BH) * np) return;  // the warp's rows all lie past the end
+  const long long bh = base / np;
+  const int i0 = static_cast<int>(base - bh * np);
+  const int c = lane % S::G, sub = lane / S::G;
+  const bool lane_on = c < S::CH;
+  uint4 ov[S::U], gv[S::U];
+  float lv[S::U];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+  for (int u = 0; u < S::U; ++u) {
+    const int i = i0 + u * S::RPW + sub;
+    ov[u] = gv[u] = make_uint4(0u, 0u, 0u, 0u);
+    lv[u] = 0.f;
+    if (lane_on && i < N) {
+      const long long src = (bh * N + i) * D + 8 * c;
+      ov[u] = __ldg(reinterpret_cast<const uint4*>(o + src));
+      gv[u] = __ldg(reinterpret_cast<const uint4*>(dO + src));
+      if (c == 0) lv[u] = __ldg(lse + bh * N + i);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < S::U; ++u) {
+    const int i = i0 + u * S::RPW + sub;
+    if (lane_on && i < N) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + (bh * N + i) * D + 8 * c);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < S::U; ++u) {
+    const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+    const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv[u]);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
       const float2 a = __bfloat1622float2(op[e]);
       const float2 b = __bfloat1622float2(gp[e]);
       acc = fmaf(a.x, b.x, acc);
       acc = fmaf(a.y, b.y, acc);
     }
-  }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    if (split) {
-      reinterpret_cast<uint4*>(lse2)[row] = bf16_split3_row(-lse[bh * N + i] * inv_scale);
-      reinterpret_cast<uint4*>(dsum)[row] = bf16_split3_row(-acc);
-    } else {
-      dsum[row] = -acc;
-      lse2[row] = -lse[bh * N + i] * 1.4426950408889634f;
+    for (int sft = S::G / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+    const int i = i0 + u * S::RPW + sub;
+    if (c == 0) {
+      const long long row = bh * np + i;  // padded row index
+      if (kSplit) {
+        // padding rows: -lse / scale far below any logit, so their P underflows to 0
+        reinterpret_cast<uint4*>(lse2)[row] = bf16_split3_row(i < N ? -lv[u] * inv_scale : -1e30f);
+        reinterpret_cast<uint4*>(dsum)[row] = bf16_split3_row(i < N ? -acc : 0.f);
+      } else {
+        lse2[row] = i < N ? -lv[u] * 1.4426950408889634f : -INFINITY;
+        dsum[row] = i < N ? -acc : 0.f;
+      }
     }
   }
-  float4* z = reinterpret_cast<float4*>(dq_acc + src);
-  for (int c = lane; c < d / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dQ = bf16(scale * acc), 8 elements per thread; threads past the n8 groups
@@ -169,13 +196,27 @@ size_t bwd_workspace_layout(int BH, int N, int d, size_t* off_lse2, size_t* off_
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t s) {
   const long long rows = static_cast<long long>(p.BH) * npad128(p.N);
-  const long long row_blocks = (rows + 7) / 8;
+  const int rb = p.d == 64 ? PrepShape<64>::RB : PrepShape<128>::RB;
+  static_assert(PrepShape<96>::RB == PrepShape<128>::RB, "d = 96 and 128 share a block shape");
+  const long long row_blocks = (rows + rb - 1) / rb;
   const long long part4 = static_cast<long long>(p.n_split) * 2 * 128 * p.d / 4;
   const long long blocks = row_blocks + (part4 + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dO), p.lse, p.lse2, p.dsum,
-      p.dq_acc, p.BH, p.N, p.d, 1.f / p.scale, p.d == 64, row_blocks, p.kv_part, part4);
+  const auto o = static_cast<const __nv_bfloat16*>(p.o);
+  const auto dO = static_cast<const __nv_bfloat16*>(p.dO);
+  const unsigned g = static_cast<unsigned>(blocks);
+  const float inv = 1.f / p.scale;
+  if (p.d == 64)
+    fa_bwd_prep_kernel<64><<<g, 256, 0, s>>>(o, dO, p.lse, p.lse2, p.dsum, p.dq_acc, p.BH, p.N, inv, row_blocks,
+                                             p.kv_part, part4);
+  else if (p.d == 96)
+    fa_bwd_prep_kernel<96><<<g, 256, 0, s>>>(o, dO, p.lse, p.lse2, p.dsum, p.dq_acc, p.BH, p.N, inv, row_blocks,
+                                             p.kv_part, part4);
+  else if (p.d == 128)
+    fa_bwd_prep_kernel<128><<<g, 256, 0, s>>>(o, dO, p.lse, p.lse2, p.dsum, p.dq_acc, p.BH, p.N, inv, row_blocks,
+                                              p.kv_part, part4);
+  else
+    return cudaErrorNotSupported;
   return cudaGetLastError();
 }
 
