@@ -87,30 +87,73 @@ struct Bars {
   __device__ uint32_t pv_done(int b) const { return base + 8 * (15 + b); }
 };
 
+// hi / lo rows of DP columns (zero past d): 16-byte chunks, four per thread
+// (256 apart, so each pass is one coalesced sweep), every load issued before
+// any is used.  The rows of x start on 16-byte boundaries when d % 4 == 0;
+// otherwise each element is read alone.
+template <int DP>
 __global__ void __launch_bounds__(256) fa_split_rows_kernel(const float* __restrict__ x, float* __restrict__ hi,
-                                                            float* __restrict__ lo, long long rows, int d, int dp) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows * dp) return;
-  const long long r = i / dp;
-  const int c = static_cast<int>(i % dp);
-  const float v = c < d ? x[r * d + c] : 0.f;
-  const float h = tf32_rna(v);
-  hi[i] = h;
-  lo[i] = tf32_rna(v - h);
+                                                            float* __restrict__ lo, long long n4, int d) {
+  constexpr int C4 = DP / 4;  // chunks per row, a power of two
+  const long long b0 = static_cast<long long>(blockIdx.x) * 1024 + threadIdx.x;
+  const bool vec = (d & 3) == 0;
+  float4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long i4 = b0 + u * 256;
+    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i4 >= n4) continue;
+    const long long r = i4 / C4;
+    const int c = static_cast<int>(i4 % C4) * 4;
+    const float* src = x + r * d + c;
+    if (vec) {
+      if (c < d) v[u] = __ldg(reinterpret_cast<const float4*>(src));
+    } else {
+      if (c < d) v[u].x = __ldg(src);
+      if (c + 1 < d) v[u].y = __ldg(src + 1);
+      if (c + 2 < d) v[u].z = __ldg(src + 2);
+      if (c + 3 < d) v[u].w = __ldg(src + 3);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long i4 = b0 + u * 256;
+    if (i4 >= n4) continue;
+    const float4 h = make_float4(tf32_rna(v[u].x), tf32_rna(v[u].y), tf32_rna(v[u].z), tf32_rna(v[u].w));
+    reinterpret_cast<float4*>(hi)[i4] = h;
+    reinterpret_cast<float4*>(lo)[i4] = make_float4(tf32_rna(v[u].x - h.x), tf32_rna(v[u].y - h.y),
+                                                    tf32_rna(v[u].z - h.z), tf32_rna(v[u].w - h.w));
+  }
 }
 
+// V^T hi / lo, [B*H][dp][npad] (zero past d and N), through a shared-memory
+// tile of 64 keys x 32 columns: read along the columns of V's rows, written
+// along the keys of V^T's rows, both coalesced.  Block (32, 8).
 __global__ void __launch_bounds__(256) fa_split_vt_kernel(const float* __restrict__ v, float* __restrict__ hi,
-                                                          float* __restrict__ lo, long long BH, int N, int npad, int d,
-                                                          int dp) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= BH * dp * npad) return;
-  const long long bh = i / (static_cast<long long>(dp) * npad);
-  const long long rem = i % (static_cast<long long>(dp) * npad);
-  const int c = static_cast<int>(rem / npad), n = static_cast<int>(rem % npad);
-  const float x = (c < d && n < N) ? v[(bh * N + n) * d + c] : 0.f;
-  const float h = tf32_rna(x);
-  hi[i] = h;
-  lo[i] = tf32_rna(x - h);
+                                                          float* __restrict__ lo, int N, int npad, int d, int dp) {
+  __shared__ float tile[64][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int nt = npad / 64, ct = dp / 32;
+  const long long blk = blockIdx.x;
+  const long long bh = blk / (static_cast<long long>(nt) * ct);
+  const int rem = static_cast<int>(blk % (static_cast<long long>(nt) * ct));
+  const int c0 = (rem / nt) * 32, n0 = (rem % nt) * 64;
+  const int c = c0 + tx;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int n = n0 + ty + 8 * j;
+    tile[ty + 8 * j][tx] = (n < N && c < d) ? __ldg(v + (bh * N + n) * d + c) : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int cc = ty + 8 * j, nn = 2 * tx;
+    const float x0 = tile[nn][cc], x1 = tile[nn + 1][cc];
+    const float h0 = tf32_rna(x0), h1 = tf32_rna(x1);
+    const long long o = ((bh * dp + c0 + cc) * npad + n0 + nn) / 2;
+    reinterpret_cast<float2*>(hi)[o] = make_float2(h0, h1);
+    reinterpret_cast<float2*>(lo)[o] = make_float2(tf32_rna(x0 - h0), tf32_rna(x1 - h1));
+  }
 }
 
 struct TcMaps {
@@ -485,15 +528,19 @@ cudaError_t launch_fwd_f32_tc(const FwdParams& p, void* workspace, EncodeTiledFn
   for (int i = 0; i < 6; ++i) buf[i] = reinterpret_cast<float*>(ws + off[i]);
   const long long rows = static_cast<long long>(p.BH) * p.N;
   const int npad = (p.N + 63) & ~63;
-  const long long n1 = rows * dp, n2 = static_cast<long long>(p.BH) * dp * npad;
-  if ((n1 + 255) / 256 > 0x7fffffffLL || (n2 + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (dp == D)
-    fa_split_rows_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.q),
-                                                                                  buf[0], buf[1], rows, p.d, dp);
-  fa_split_rows_kernel<<<static_cast<unsigned>((n1 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.k), buf[2],
-                                                                                buf[3], rows, p.d, dp);
-  fa_split_vt_kernel<<<static_cast<unsigned>((n2 + 255) / 256), 256, 0, s>>>(static_cast<const float*>(p.v), buf[4],
-                                                                              buf[5], p.BH, p.N, npad, p.d, dp);
+  const long long n4 = rows * dp / 4, b1 = (n4 + 1023) / 1024;
+  const long long b2 = static_cast<long long>(p.BH) * (npad / 64) * (dp / 32);
+  if (b1 > 0x7fffffffLL || b2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const auto split_rows = [&](const void* x, float* h, float* l) {
+    if (dp == D)
+      fa_split_rows_kernel<D><<<static_cast<unsigned>(b1), 256, 0, s>>>(static_cast<const float*>(x), h, l, n4, p.d);
+    else
+      fa_split_rows_kernel<128><<<static_cast<unsigned>(b1), 256, 0, s>>>(static_cast<const float*>(x), h, l, n4, p.d);
+  };
+  if (dp == D) split_rows(p.q, buf[0], buf[1]);
+  split_rows(p.k, buf[2], buf[3]);
+  fa_split_vt_kernel<<<static_cast<unsigned>(b2), 256, 0, s>>>(static_cast<const float*>(p.v), buf[4], buf[5], p.N,
+                                                               npad, p.d, dp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const uint64_t BH = static_cast<uint64_t>(p.BH), Nn = static_cast<uint64_t>(p.N);
