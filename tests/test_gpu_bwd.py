@@ -154,6 +154,57 @@ def test_bwd_guard_bands(d):
         _check_grad(name, _np(g), r, d)
 
 
+@pytest.mark.parametrize("d", [64, 96, 128])
+def test_bwd_workspace_rows(d):
+    """White-box check of the element-wise passes around the main kernel, on a
+    workspace the caller supplies (its layout is the one fa.h documents).
+    Every row's lse term is -lse log2 e (d = 64: -lse / scale) and its D term is
+    -D_i = -sum_k dO_ik O_ik, computed here in float64 from the same O, lse
+    and dO.  The padding rows past N hold the values that make their P (and
+    so their dS) zero.  And dQ is exactly bf16(scale * accumulator).  A wrong
+    term on a few rows would barely move the gradients' relative L2 error;
+    here every row is checked."""
+    dev = _dev()
+    fa = _fa()
+    B, H, N = 2, 3, 300  # Npad = 384: 84 padding rows per head
+    q, k, v, do = (t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=31, with_do=True))
+    scale = 1 / np.sqrt(d)
+    o, lse = fa.fa_fwd(q, k, v, scale=scale)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), device=dev, dtype=torch.uint8)
+    dq, _, _ = fa.fa_bwd(q, k, v, o, lse, do, scale=scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    raw = ws.cpu().numpy()
+    npad = (N + 127) // 128 * 128
+    acc_bytes = (B * H * N * d * 4 + 255) // 256 * 256
+    per = 16 if d == 64 else 4
+    vec_bytes = (B * H * npad * per + 255) // 256 * 256
+
+    def section(off):
+        if d == 64:  # three bf16 terms and five zeros per 16-byte row
+            u16 = raw[off:off + B * H * npad * 16].view(np.uint16).reshape(B * H, npad, 8)
+            assert np.all(u16[..., 3:] == 0)
+            terms = (u16[..., :3].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            return terms.sum(-1)
+        return raw[off:off + B * H * npad * 4].view(np.float32).reshape(B * H, npad).astype(np.float64)
+
+    lterm, dterm = section(acc_bytes), section(acc_bytes + vec_bytes)
+    od, dod = _np(o).reshape(B * H, N, d), _np(do).reshape(B * H, N, d)
+    want_d = -(od * dod).sum(-1)
+    mag = (np.abs(od) * np.abs(dod)).sum(-1)
+    L = lse.cpu().numpy().astype(np.float64).reshape(B * H, N)
+    want_l = -L / np.float32(scale) if d == 64 else -L * np.log2(np.e)
+    assert np.all(np.abs(lterm[:, :N] - want_l) <= 2e-6 * np.abs(want_l) + 1e-6)
+    assert np.all(np.abs(dterm[:, :N] - want_d) <= 1e-5 * mag + 1e-7)
+    if d == 64:
+        assert np.all(np.abs(lterm[:, N:] + 1e30) <= 1e-6 * 1e30)
+    else:
+        assert np.all(lterm[:, N:] == -np.inf)
+    assert np.all(dterm[:, N:] == 0.0)
+    acc = torch.from_numpy(raw[:B * H * N * d * 4].view(np.float32).reshape(B, H, N, d).copy())
+    assert torch.equal((acc * np.float32(scale)).to(torch.bfloat16), dq.cpu())
+
+
 @pytest.mark.parametrize("d", [64, 96])
 def test_bwd_large_sampled_heads(d):
     """d = 64 and 96 at a size with many key and query tiles (B=2, H=8,
