@@ -1,0 +1,76 @@
+"""GPU parity beyond 32-bit element offsets: B*H*N*d just over 2^31 per
+tensor (4 GB of bf16 each; about 45 GB on the device in all), forward and
+backward through the C ABI, at the head dimensions of the headline kernels.
+
+Heads at the start, middle and end of the batch are compared with the
+float64 oracle (O, lse, dQ, dK, dV), and every output is checked finite.  An
+offset computed in 32 bits anywhere would put the last heads' rows in the
+wrong place or read the wrong rows.
+
+Inputs: 64 seeded heads from the shared input generator.  Head h of the large
+problem is base head h mod 64, rotated by h // 64 positions along the sequence,
+so every head differs.  The oracle rebuilds the sampled heads on the CPU from
+the same base.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+N = 256
+BASE_HEADS = 64
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_more_than_2_31_elements_per_tensor(d):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_tiled_attention_02_gb300 import binding as fa
+    dev = torch.device("cuda:0")
+    H = (1 << 31) // (N * d) + 1  # B*H*N*d = 2^31 + N*d
+    base = inputs.make_inputs(1, BASE_HEADS, N, d, "bf16", seed=77, with_do=True)
+
+    hs = torch.arange(H, device=dev)
+    idx = (torch.arange(N, device=dev)[None, :] - (hs // BASE_HEADS)[:, None]) % N
+
+    def expand(t):
+        return t[0].to(dev)[(hs % BASE_HEADS)[:, None], idx].unsqueeze(0)
+
+    def head(t, h):
+        return torch.roll(t[0, h % BASE_HEADS], shifts=h // BASE_HEADS, dims=0)
+
+    q, k, v, do = (expand(t) for t in base)
+    assert q.numel() > (1 << 31)
+    scale = 1 / np.sqrt(d)
+    o, lse = fa.fa_fwd(q, k, v, scale=scale)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for t in (o, dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    assert bool(torch.isfinite(lse).all())
+    for h in (0, H // 2, H - 1):
+        qh, kh, vh, doh = (_np(head(t, h)) for t in base)
+        o_ref, lse_ref = oracle.dense_forward(qh, kh, vh, scale)
+        err = np.abs(_np(o[0, h]) - o_ref)
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (h, err.max(), err.mean())
+        assert np.abs(lse[0, h].cpu().numpy().astype(np.float64) - lse_ref).max() <= 1e-3, h
+        refs = oracle.dense_backward(qh, kh, vh, doh, scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[0, h], dk[0, h], dv[0, h]), refs):
+            assert _rel(_np(g), r) <= 1e-2, (name, h, _rel(_np(g), r))
+    del q, k, v, do, o, lse, dq, dk, dv, idx, hs
+    torch.cuda.empty_cache()
