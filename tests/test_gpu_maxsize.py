@@ -1,7 +1,7 @@
 """GPU parity beyond 32-bit element offsets: B*H*N*d just over 2^31 per
-tensor, forward and backward through the C ABI, in bf16 at the head
-dimensions of the headline kernels, with and without a window (4 GB per
-tensor, about 45 GB on the device) and in float32 on both float32 forward paths (8.6 GB per tensor).
+tensor, forward and backward through the C ABI, in bf16 at every head
+dimension, with and without a window (4 GB per tensor, about 45 GB on the
+device; d = 256 forward only) and in float32 on both float32 forward paths (8.6 GB per tensor).
 
 Heads at the start, middle and end of the batch are compared with the
 float64 oracle (O, lse, dQ, dK, dV), and every output is checked finite.  An
@@ -36,7 +36,7 @@ def _rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-@pytest.mark.parametrize("d,window", [(64, 0), (128, 0), (128, 257)])
+@pytest.mark.parametrize("d,window", [(64, 0), (96, 0), (128, 0), (128, 257), (256, 0)])
 def test_more_than_2_31_elements_per_tensor(d, window):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -57,23 +57,24 @@ def test_more_than_2_31_elements_per_tensor(d, window):
     q, k, v, do = (expand(t) for t in base)
     assert q.numel() > (1 << 31)
     scale = 1 / np.sqrt(d)
+    with_bwd = d != 256  # bf16 d = 256 is forward only
     o, lse = fa.fa_fwd(q, k, v, scale=scale, window=window)
-    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, scale=scale, window=window)
+    grads = fa.fa_bwd(q, k, v, o, lse, do, scale=scale, window=window) if with_bwd else ()
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == fa.FA_OK
-    for t in (o, dq, dk, dv):
+    for t in (o, lse, *grads):
         assert bool(torch.isfinite(t).all())
-    assert bool(torch.isfinite(lse).all())
     for h in (0, H // 2, H - 1):
         qh, kh, vh, doh = (_np(head(t, h)) for t in base)
         o_ref, lse_ref = oracle.dense_forward(qh, kh, vh, scale, window)
         err = np.abs(_np(o[0, h]) - o_ref)
         assert err.max() <= 2e-2 and err.mean() <= 2e-3, (h, err.max(), err.mean())
         assert np.abs(lse[0, h].cpu().numpy().astype(np.float64) - lse_ref).max() <= 1e-3, h
-        refs = oracle.dense_backward(qh, kh, vh, doh, scale, window)
-        for name, g, r in zip(("dq", "dk", "dv"), (dq[0, h], dk[0, h], dv[0, h]), refs):
-            assert _rel(_np(g), r) <= 1e-2, (name, h, _rel(_np(g), r))
-    del q, k, v, do, o, lse, dq, dk, dv, idx, hs
+        if with_bwd:
+            refs = oracle.dense_backward(qh, kh, vh, doh, scale, window)
+            for name, g, r in zip(("dq", "dk", "dv"), (t[0, h] for t in grads), refs):
+                assert _rel(_np(g), r) <= 1e-2, (name, h, _rel(_np(g), r))
+    del q, k, v, do, o, lse, grads, idx, hs
     torch.cuda.empty_cache()
 
 
