@@ -710,8 +710,9 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         // this tile's S buffer and the phase it completes there
         int sb = t;
         uint32_t sph = n & 1;
+        int k = 0;  // (three-buffer layout) index of this S product among all issued
         if constexpr (tri_s<D, WIN>()) {
-          const int k = pair ? ks + 2 * it + t : ks + it;
+          k = pair ? ks + 2 * it + t : ks + it;
           sb = k % 3;
           sph = (k / 3) & 1;
         }
@@ -787,9 +788,22 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         }
         const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y) + (rs[2].x + rs[2].y) + (rs[3].x + rs[3].y);
         // O may be rescaled only once this item's previous P V into it has
-        // completed (the first tile of an item starts a fresh O)
+        // completed (the first tile of an item starts a fresh O).  With one S
+        // buffer per tile at most that P V is outstanding, and o_done's
+        // parity names it.  With three buffers a single tile can have two
+        // outstanding (its S was issued once the P V three back completed),
+        // and a parity wait on o_done would then return on the older phase.
+        // So there the wait is on pv_done of the previous P's buffer, which
+        // has at most one use outstanding; P V products complete in issue
+        // order, so that P V's completion implies every earlier one's.
         if (!corr_warps<D, WIN>() && it > w.lo[t] && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
+          uint32_t pb = bar.o_done(t), pp = (n - 1) & 1;
+          if constexpr (tri_s<D, WIN>()) {
+            const int kp = k - (pair ? 2 : 1);
+            pb = bar.pv_done(kp % 3);
+            pp = (kp / 3) & 1;
+          }
+          if (!warp_wait(pb, pp)) {
             tmem_wait_st();
             ok = false;
             break;
@@ -837,9 +851,19 @@ __global__ void __launch_bounds__(threads_for<D, WIN>(), 1)
         }
       }
       // wait for this item's last P V (the next item's first P V into O needs
-      // this warpgroup's first P of that item, so it cannot have started)
+      // this warpgroup's first P of that item, so it cannot have started).
+      // Three-buffer layout: up to three of this tile's P V products may still
+      // be outstanding here (two for a tile of a pair), so, as for the
+      // rescale, the wait is on pv_done of the tile's last P (ks already
+      // counts this item's S products).
       if (w.lo[t] < w.hi[t]) {
-        if (!warp_wait(bar.o_done(t), (n - 1) & 1)) {
+        uint32_t eb = bar.o_done(t), ep = (n - 1) & 1;
+        if constexpr (tri_s<D, WIN>()) {
+          const int kl = ks - (pair ? 2 - t : 1);
+          eb = bar.pv_done(kl % 3);
+          ep = (kl / 3) & 1;
+        }
+        if (!warp_wait(eb, ep)) {
           ok = false;
           break;
         }
