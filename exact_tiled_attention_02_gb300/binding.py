@@ -1,14 +1,16 @@
 """Python binding of libfa.so (the C ABI in include/fa.h).
 
 Argument marshalling only: torch tensors become device pointers and sizes,
-the current torch CUDA stream becomes the ``stream`` argument, and non-OK
-status codes become ``FaError``.  Every step of attention runs in the
-library's CUDA kernels; there is no other code path.  PyTorch supplies device
-memory (outputs and the backward's workspace) and streams.
+the ``stream`` keyword (a torch CUDA stream; by default the current one)
+becomes the library's stream argument, and non-OK status codes become
+``FaError``.  Every step of attention runs in the library's CUDA kernels;
+there is no other code path.  PyTorch supplies device memory (outputs and
+workspaces, allocated on the stream the call runs on) and streams.
 """
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -79,6 +81,16 @@ def _stream_ptr(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _alloc_on(stream):
+    """Context for the tensors a call allocates (outputs, workspace): on the
+    stream its kernels run on.  The caching allocator hands a freed block out
+    again in the order of the stream it was allocated on; a workspace
+    allocated on the current stream and dropped on return, while the kernels
+    still run on another stream, could otherwise be reused at once."""
+    torch = _torch()
+    return contextlib.nullcontext() if stream is None else torch.cuda.stream(stream)
 
 
 def _dtype_code(t) -> int:
@@ -154,12 +166,12 @@ def fa_fwd(q, k, v, scale: float | None = None, window: int = 0, o=None, lse=Non
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _check_qkv(q, o)
-    if lse is None and want_lse:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with _alloc_on(stream):
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    _check_qkv(q, o)
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N):
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(window),
@@ -181,16 +193,16 @@ def fa_fwd_key_major(q, k, v, scale: float | None = None, window: int = 0, o=Non
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _check_qkv(q, o)
-    if lse is None and want_lse:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with _alloc_on(stream):
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+        if workspace is None:
+            workspace = torch.empty(fa_fwd_key_major_workspace_bytes(B, H, N, d), device=q.device, dtype=torch.uint8)
+    _check_qkv(q, o)
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N):
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
-    if workspace is None:
-        workspace = torch.empty(fa_fwd_key_major_workspace_bytes(B, H, N, d), device=q.device, dtype=torch.uint8)
     st = lib.fa_fwd_key_major(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(window),
                               _dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream_ptr(stream))
@@ -213,16 +225,16 @@ def fa_fwd_f32_3xtf32(q, k, v, scale: float | None = None, window: int = 0, o=No
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _check_qkv(q, o)
-    if lse is None and want_lse:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with _alloc_on(stream):
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+        if workspace is None:
+            workspace = torch.empty(fa_fwd_f32_3xtf32_workspace_bytes(B, H, N, d), device=q.device, dtype=torch.uint8)
+    _check_qkv(q, o)
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N):
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
-    if workspace is None:
-        workspace = torch.empty(fa_fwd_f32_3xtf32_workspace_bytes(B, H, N, d), device=q.device, dtype=torch.uint8)
     st = lib.fa_fwd_f32_3xtf32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(window),
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != FA_OK:
@@ -246,13 +258,14 @@ def fa_bwd(q, k, v, o, lse, do, scale: float | None = None, window: int = 0, dq=
         scale = 1.0 / math.sqrt(d)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * N:
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    _check_qkv(q, dq, dk, dv)
     need = fa_bwd_workspace_bytes(B, H, N, d)
-    if workspace is None:
-        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    with _alloc_on(stream):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(q) if dk is None else dk
+        dv = torch.empty_like(q) if dv is None else dv
+        if workspace is None:
+            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    _check_qkv(q, dq, dk, dv)
     st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                     B, H, N, d, float(scale), int(window), _dtype_code(q), _ptr(workspace),
                     workspace.numel() * workspace.element_size(), _stream_ptr(stream))

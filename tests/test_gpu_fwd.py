@@ -327,3 +327,38 @@ def test_binding_rejects_bad_tensors():
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd(x, x, x)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+def test_calls_run_on_the_given_stream():
+    """Every call runs on the stream it is given, after the work already on
+    that stream, when called from another one.  The forward, the backward
+    and the 3xTF32 forward are called from the default stream with
+    ``stream=s``, while s is still busy producing Q.  A launch on any other
+    stream would read Q before it exists.  O, lse, dK, dV and the float32
+    outputs match runs on the default stream bit for bit (dQ, summed by
+    reductions in any order, to rounding)."""
+    dev = _dev()
+    fa = _fa()
+    B, H, N, d = 2, 4, 1000, 128
+    q, k, v, do = (t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=41, with_do=True))
+    qf, kf, vf = (t.float() for t in (q, k, v))
+    o_ref, lse_ref = fa.fa_fwd(q, k, v)
+    dq_ref, dk_ref, dv_ref = fa.fa_bwd(q, k, v, o_ref, lse_ref, do)
+    o32_ref, l32_ref = fa.fa_fwd_f32_3xtf32(qf, kf, vf)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        busy = torch.randn(4096, 4096, device=dev)
+        for _ in range(30):  # tens of milliseconds of work ahead of Q on s
+            busy = (busy @ busy).mul_(1e-3)
+        q2, qf2 = q.clone(), qf.clone()
+    o, lse = fa.fa_fwd(q2, k, v, stream=s)
+    dq, dk, dv = fa.fa_bwd(q2, k, v, o, lse, do, stream=s)
+    o32, l32 = fa.fa_fwd_f32_3xtf32(qf2, kf, vf, stream=s)
+    assert fa.fa_last_device_status(stream=s) == fa.FA_OK
+    s.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    assert torch.equal(dk, dk_ref) and torch.equal(dv, dv_ref)
+    assert float((dq.float() - dq_ref.float()).norm() / dq_ref.float().norm()) <= 1e-3
+    assert torch.equal(o32, o32_ref) and torch.equal(l32, l32_ref)
