@@ -69,3 +69,37 @@ def test_static_workspace_binding_checks_lse():
     for bad in (good.half(), good[:, :1], torch.zeros(1, 256, 2, device=dev).transpose(1, 2)):
         with pytest.raises(ValueError):
             fa.fa_bwd_static_workspace(x, x, x, x, bad, x, x, x, x)
+
+
+def test_static_workspace_in_a_cuda_graph():
+    """What the entry point is for: a backward inside a captured CUDA graph
+    with nothing allocated for it.  Captured once after a warm-up call,
+    replayed on new inputs, it matches fa_bwd with an ordinary workspace (dK,
+    dV bit for bit, dQ to rounding)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_tiled_attention_02_gb300 import binding as fa
+    dev = torch.device("cuda:0")
+    B, H, N, d = 1, 2, 700, 128
+    q, k, v, do = (t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=60, with_do=True))
+    o, lse = fa.fa_fwd(q, k, v)
+    out = tuple(torch.empty_like(q) for _ in range(3))
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fa.fa_bwd_static_workspace(q, k, v, o, lse, do, *out)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.fa_bwd_static_workspace(q, k, v, o, lse, do, *out)
+    new = [t.to(dev) for t in inputs.make_inputs(B, H, N, d, "bf16", seed=61, with_do=True)]
+    o_new, lse_new = fa.fa_fwd(*new[:3])
+    for dst, src in zip((q, k, v, do, o, lse), (*new, o_new, lse_new)):
+        dst.copy_(src)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    ref = fa.fa_bwd(*new[:3], o_new, lse_new, new[3])
+    torch.cuda.synchronize()
+    assert torch.equal(out[1], ref[1]) and torch.equal(out[2], ref[2])  # dK, dV: reduced on chip
+    assert _rel(out[0], ref[0]) <= 1e-3
