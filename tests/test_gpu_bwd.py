@@ -85,6 +85,11 @@ BWD_CASES = [
     (1, 2, 200, 96, 0, 1.0),
     (1, 1, 513, 96, 0, 8.0),
     (1, 2, 700, 96, 65, 1.0),
+    # bands wider than one key tile each side: each key tile meets several
+    # query tiles through the band-limited loop
+    (1, 1, 2000, 128, 1025, 1.0),
+    (1, 2, 1500, 96, 513, 8.0),
+    (1, 1, 1800, 64, 769, 1.0),
 ]
 
 
